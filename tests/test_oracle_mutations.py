@@ -1,0 +1,109 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and show a pin catches each.
+
+Every mutation below is a mistake that could slip into a restatement of the
+method: a transposed operand, a wrong row index, a tie-break flipped, an
+off-by-one in the commit, a dropped temperature, a non-strict comparison.  The
+pins of ``oracle_checks`` must fail on every one of them.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.verify as ov
+import oracle_checks as oc
+
+
+def _argmax_last(row):
+    return int(len(row) - 1 - np.argmax(row[::-1]))
+
+
+def _residual_transposed(p, q):
+    return np.maximum(0.0, q - p)
+
+
+def _accept_transposed(u, p_d, q_d):
+    return u < min(1.0, q_d / p_d if p_d > 0 else np.inf)
+
+
+def _accept_without_clamp(u, p_d, q_d):
+    return u < 0.5 * min(1.0, ov.acceptance_ratio(p_d, q_d)) + 0.25
+
+
+def _greedy_next_row(t_rows, drafts):
+    k = len(drafts)
+    a = [ov.argmax_lowest(r) for r in t_rows]
+    n = 0
+    while n < k and int(drafts[n]) == a[min(n + 1, k)]:
+        n += 1
+    return a[:n + 1]
+
+
+def _softmax_no_temperature(row, temperature):
+    z = row
+    zmax = np.max(z)
+    e = np.exp(z - zmax)
+    return e / e.sum(), float(zmax + np.log(e.sum()))
+
+
+def _inverse_cdf_non_strict(weights, u):
+    cdf = np.cumsum(weights)
+    target = u * cdf[-1]
+    token = int(np.nonzero(cdf >= target)[0][0])
+    return token, 1.0
+
+
+def _row_budget_ceil(draft_tokens, rows, lanes):
+    rows = rows or 8
+    return max(0, min(draft_tokens, -(-rows // lanes) - 1))
+
+
+def _commit_wrong_column(staged, live, committed, lane_status=None):
+    out = np.array(live, copy=True)
+    for b in range(staged.shape[0]):
+        c = int(committed[b])
+        if 1 <= c <= staged.shape[1]:
+            out[b] = staged[b, min(c, staged.shape[1] - 1)]
+    return out
+
+
+MUTATIONS = [
+    ("argmax ties to the highest index", ov, "argmax_lowest", _argmax_last,
+     oc.check_greedy_equals_plain_decode),
+    ("residual max(0, q - p)", ov, "residual_weights", _residual_transposed,
+     oc.check_sampled_exact_enumeration),
+    ("acceptance ratio q/p", ov, "accept_draft", _accept_transposed,
+     oc.check_sampled_exact_enumeration),
+    ("acceptance threshold distorted", ov, "accept_draft", _accept_without_clamp,
+     oc.check_sampled_monte_carlo),
+    ("greedy compares d_{j+1} with row j+1", ov, "_greedy_lane", _greedy_next_row,
+     oc.check_guess_check_table),
+    ("temperature dropped", ov, "softmax_at_temperature", _softmax_no_temperature,
+     oc.check_sampled_exact_enumeration),
+    ("inverse CDF with >=", ov, "inverse_cdf", _inverse_cdf_non_strict,
+     oc.check_inverse_cdf_never_draws_zero_weight),
+    ("row budget rounds up", oracle, "row_budget", _row_budget_ceil,
+     oc.check_row_budget_worked_example),
+    ("commit copies column c", oracle, "commit_state", _commit_wrong_column,
+     oc.check_commit_copies_column_committed_minus_one),
+]
+
+
+@pytest.mark.parametrize("what,module,name,bad,check", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(monkeypatch, what, module, name, bad, check):
+    monkeypatch.setattr(module, name, bad)
+    with pytest.raises(AssertionError):
+        check()
+
+
+def test_commit_mistake_breaks_no_trace(monkeypatch):
+    monkeypatch.setattr(oracle, "commit_state", _commit_wrong_column)
+    with pytest.raises(AssertionError):
+        oc.check_greedy_equals_plain_decode()
+
+
+def test_philox_round_count_matters(monkeypatch):
+    import oracle.philox as ph
+    monkeypatch.setattr(ph, "ROUNDS", 9)
+    with pytest.raises(AssertionError):
+        oc.check_philox_against_numpy()
