@@ -1,0 +1,554 @@
+#!/usr/bin/env python
+"""Verify-round benchmark on GB300: verified logit rows/s and achieved HBM GB/s.
+
+A step is one verify round over one batch of synthetic input: the row budget
+(host), the fused verify-accept kernel and, for workloads with recurrent
+state, the state commit.  Steps run from a captured CUDA graph (the kernels
+take microseconds, so launching them one by one from Python would measure the
+launcher); consecutive steps rotate over enough input sets that a set's logits
+have left the 129 MB L2 before it comes round again.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Under torchrun (N > 1) every rank verifies its own batch (lanes are
+independent, so there is no collective on the data path); the time is the
+maximum over ranks and ``value`` counts the rows of all ranks.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "verified logit rows/sec and achieved HBM GB/s (% of GB300 peak) per verify round"
+UNIT = "rows/s"
+L2_BYTES = 129 * 2 ** 20
+DEFAULT_WORKLOAD = workloads.GREEDY_B8
+GRAPH_STEPS = 500          # steps per captured graph
+SOAK_SECONDS = 1.0         # untimed replays before the timed region (clocks settle, samples exist)
+FALLBACK_HBM_GBS = 6800.0  # used only if MEASURED_PEAKS.json is absent
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verify_bf16_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    with open(os.path.join(ROOT, "include", "spec_verify.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(float(fields["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.device_index)],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def round_bytes(r):
+    """Algorithmic bytes of one verify launch: logits rows read, metadata, outputs."""
+    lens = r.draft_lens.cpu().numpy().astype(np.int64)
+    temps = r.temperatures.cpu().numpy()
+    esize = r.target.element_size()
+    target_rows = int((lens + 1).sum())
+    draft_rows = int(lens[temps > 0].sum())
+    logits = (target_rows + draft_rows) * r.vocab * esize
+    meta = 4 * (r.rows + r.lanes + (r.lanes + 1) + r.lanes)   # tokens, lens, offsets, temps
+    out = 4 * (r.lanes + r.rows + r.lanes)                     # committed, out_tokens, status
+    return logits + meta + out, target_rows
+
+
+def commit_bytes(r):
+    per_lane = r.live[0].numel() * r.live.element_size()
+    return 2 * per_lane * r.lanes + 8 * r.lanes
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class Bench:
+    def __init__(self, name, seed, device, rank):
+        import speculative_decoding_verify_bf16_gb300 as sv
+        self.sv = sv
+        self.name = name
+        self.device = device
+        first = workloads.make_round(name, seed=seed + 1000 * rank, device=device)
+        set_bytes = first.logits_bytes()
+        n_sets = max(2, math.ceil(1.5 * L2_BYTES / set_bytes) + 1)
+        n_sets = min(n_sets, 16)
+        self.sets = [first] + [workloads.make_round(name, seed=seed + 1000 * rank + i, device=device,
+                                                    with_state=False)
+                               for i in range(1, n_sets)]
+        if first.staged is not None:
+            for s in self.sets[1:]:  # one recurrent state, shared: its reads dwarf L2 anyway
+                s.staged, s.live = first.staged, first.live
+        self.set_bytes = set_bytes
+        self.outs = []
+        for s in self.sets:
+            self.outs.append(dict(
+                committed=torch.zeros(s.lanes, dtype=torch.int32, device=device),
+                out_tokens=torch.zeros(s.rows, dtype=torch.int32, device=device),
+                status=torch.zeros(s.lanes, dtype=torch.int32, device=device)))
+        self.args = [sv.make_args(s.target, s.draft, s.draft_tokens, s.draft_lens, s.row_offsets,
+                                  s.temperatures, s.seed, o["committed"], o["out_tokens"], o["status"],
+                                  rows=s.rows)
+                     for s, o in zip(self.sets, self.outs)]
+        self.verify_bytes, self.rows_per_step = round_bytes(first)
+        self.has_state = first.staged is not None
+        self.commit_bytes = commit_bytes(first) if self.has_state else 0
+        self.launches_per_step = 1 + (1 if self.has_state else 0)
+
+    def check_budget(self):
+        r = self.sets[0]
+        if self.name == workloads.RAGGED_MIXED_B128:
+            k = self.sv.spec_row_budget(workloads.RAGGED_DRAFT_TOKENS, workloads.RAGGED_ROW_BUDGET, r.lanes)
+            assert k == workloads.RAGGED_DRAFT_TOKENS and r.rows <= workloads.RAGGED_ROW_BUDGET
+        else:
+            k = int(r.draft_lens.max())
+            assert self.sv.spec_row_budget(k, r.rows, r.lanes) == k
+
+    def step(self, i, stream, verify=True, commit=True):
+        j = i % len(self.sets)
+        s = self.sets[j]
+        h = stream.cuda_stream
+        import ctypes
+        if verify:
+            code = self.sv.spec_verify_accept_raw(self.args[j], ctypes.c_void_p(h))
+            if code != 0:
+                raise RuntimeError(f"spec_verify_accept: {code}")
+        if commit and self.has_state:
+            self.sv.spec_commit_state(s.staged, s.live, self.outs[j]["committed"], self.outs[j]["status"],
+                                      stream=stream)
+
+    def capture(self, steps, stream, **kw):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(steps):
+                    self.step(i, torch.cuda.current_stream(), **kw)
+        return g
+
+
+def timed_graph_run(bench, K, stream, world, **kw):
+    """Replay graphs for exactly K steps; returns elapsed ms (events on `stream`)."""
+    g_full = bench.capture(min(K, GRAPH_STEPS), stream, **kw)
+    rem = K % GRAPH_STEPS if K > GRAPH_STEPS else 0
+    g_rem = bench.capture(rem, stream, **kw) if rem else None
+    reps = K // GRAPH_STEPS if K > GRAPH_STEPS else 1
+    g_full.replay()  # upload
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    return start.elapsed_time(end), (g_full, g_rem, reps)
+
+
+def soak(graphs, stream, seconds):
+    g_full = graphs[0]
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        while time.time() - t0 < seconds:
+            g_full.replay()
+            torch.cuda.synchronize()
+
+
+def e2e_run(bench, steps, stream):
+    """Public API end to end: pinned host inputs -> H2D -> verify -> D2H of the result."""
+    sv = bench.sv
+    hosts = []
+    for s in bench.sets[:2]:
+        hosts.append({k: getattr(s, k).cpu().pin_memory() for k in
+                      ("target", "draft_tokens", "draft_lens", "row_offsets", "temperatures")})
+        if s.draft is not None:
+            hosts[-1]["draft"] = s.draft.cpu().pin_memory()
+    dev = {k: torch.empty_like(v, device=bench.device) for k, v in hosts[0].items()}
+    s0 = bench.sets[0]
+    committed = torch.empty(s0.lanes, dtype=torch.int32, device=bench.device)
+    out_tokens = torch.empty(s0.rows, dtype=torch.int32, device=bench.device)
+    res_c = torch.empty(s0.lanes, dtype=torch.int32).pin_memory()
+    res_t = torch.empty(s0.rows, dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in hosts[0].values())
+    d2h = res_c.numel() * 4 + res_t.numel() * 4
+
+    def one(i):
+        h = hosts[i % len(hosts)]
+        for k, v in h.items():
+            dev[k].copy_(v, non_blocking=True)
+        sv.spec_verify_accept(dev["target"], dev.get("draft"), dev["draft_tokens"], dev["draft_lens"],
+                              dev["row_offsets"], dev["temperatures"], s0.seed + i, committed,
+                              out_tokens, stream=stream)
+        res_c.copy_(committed, non_blocking=True)
+        res_t.copy_(out_tokens, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            one(i)
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(steps):
+            one(i)
+        end.record(stream)
+        torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    return ms, h2d, d2h
+
+
+def cpu_baseline(name, seed, budget_s=12.0):
+    """The oracle as it stands, on a bounded sample of the workload (rank 0 only)."""
+    import oracle
+    r = workloads.make_round(name, seed=seed, device="cpu")
+    lanes = r.lanes
+    off = r.row_offsets.numpy()
+    # Sample: as many whole lanes as fit the budget (at least one), from one round.
+    t_dec = time.time()
+    target = (oracle.decode_bf16(r.target.view(torch.int16).numpy().view(np.uint16))
+              if r.target.dtype == torch.bfloat16 else r.target.numpy().astype(np.float64))
+    draft = None
+    if r.draft is not None:
+        draft = oracle.decode_bf16(r.draft.view(torch.int16).numpy().view(np.uint16))
+    t_dec = time.time() - t_dec
+    rows_done, t_total, reps = 0, 0.0, 0
+    take = lanes
+    while t_total < budget_s:
+        t0 = time.time()
+        res = oracle.verify_round(target, draft, r.draft_tokens.numpy(), r.draft_lens.numpy()[:take],
+                                  off[:take + 1], r.temperatures.numpy()[:take], seed=r.seed)
+        dt = time.time() - t0
+        assert (res.lane_status == 0).all()
+        t_total += dt
+        rows_done += int(off[take])
+        reps += 1
+        if reps == 1 and dt > budget_s / 3 and take > 1:
+            take = max(1, int(take * budget_s / 3 / dt))
+    sample = (f"{reps} oracle round(s) over {'all ' if take == lanes else ''}{take} of {lanes} lanes "
+              f"({rows_done} rows); bf16 decode of the inputs ({t_dec:.2f} s) excluded")
+    return {"value": rows_done / t_total, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    import speculative_decoding_verify_bf16_gb300 as sv
+    sv.build_library()
+    sv.load_library()
+
+    bench = Bench(args.workload, args.seed, device, rank)
+    bench.check_budget()
+    stream = torch.cuda.Stream(device=device)
+    K, W = args.steps, args.warmup
+
+    # warm-up: W eager steps
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            bench.step(i, stream)
+    torch.cuda.synchronize()
+    st = bench.outs[0]["status"].cpu().numpy()
+    assert (st == 0).all(), st
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    ms_total, graphs = timed_graph_run(bench, K, stream, world)
+    soak(graphs, stream, SOAK_SECONDS)
+    # per-kernel timing: the same K steps with one kernel kind only
+    ms_verify, _ = timed_graph_run(bench, K, stream, world, commit=False)
+    ms_commit = None
+    if bench.has_state:
+        ms_commit, _ = timed_graph_run(bench, K, stream, world, verify=False)
+    clocks = sampler.stop()
+
+    t = torch.tensor([ms_total, ms_verify, ms_commit or 0.0], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_total, ms_verify, ms_commit = t.tolist()
+
+    e2e_ms, h2d, d2h = e2e_run(bench, max(5, min(K, 50)), stream)
+    e2e_steps = max(5, min(K, 50))
+    e2e_t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(e2e_t, op=torch.distributed.ReduceOp.MAX)
+
+    peak, peak_kind = measured_hbm_peak()
+    verify_us = ms_verify * 1e3 / K
+    verify_gbs = bench.verify_bytes / (verify_us * 1e-6) / 1e9
+    kernels = {"verify_accept": {"us_per_launch": verify_us, "algorithmic_bytes": bench.verify_bytes,
+                                 "gbs": verify_gbs, "frac_of_peak": verify_gbs / peak}}
+    dominant = "verify_accept"
+    if bench.has_state:
+        commit_us = ms_commit * 1e3 / K
+        commit_gbs = bench.commit_bytes / (commit_us * 1e-6) / 1e9
+        kernels["commit_state"] = {"us_per_launch": commit_us, "algorithmic_bytes": bench.commit_bytes,
+                                   "gbs": commit_gbs, "frac_of_peak": commit_gbs / peak}
+        if commit_us > verify_us:
+            dominant = "commit_state"
+    dk = kernels[dominant]
+    traffic = profiled_traffic(dominant, args.workload)
+    rows_total = bench.rows_per_step * K * world
+    value = rows_total / (ms_total * 1e-3)
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": ms_total / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if bench.sets[0].dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload,
+            "lanes": bench.sets[0].lanes,
+            "vocab": bench.sets[0].vocab,
+            "rows_per_step": bench.rows_per_step,
+            "logits_dtype": bench.sets[0].dtype,
+            "recurrent_state": bench.has_state,
+            "l2": (f"inputs rotate over {len(bench.sets)} sets of {bench.set_bytes / 2**20:.1f} MiB "
+                   f"logits (> 129 MB L2 between reuses)"),
+            "timing": f"CUDA-graph replays of {min(K, GRAPH_STEPS)} steps, events on the launch stream",
+            "parallelism": f"lanes sharded over {world} GPU(s)" if world > 1 else "1 GPU",
+        },
+        "hbm_gbs": {"achieved": dk["gbs"], "peak": peak, "peak_source": peak_kind},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dk["gbs"], "peak": peak,
+                     "unit": "GB/s", "frac": dk["gbs"] / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dk["algorithmic_bytes"],
+                     "us_per_launch": dk["us_per_launch"], "peak_source": peak_kind},
+        "kernels": kernels,
+        "e2e": {"value": bench.rows_per_step * e2e_steps * world / (e2e_t.item() * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "pinned host inputs -> H2D -> spec_verify_accept (python binding) -> D2H"},
+        "gpu_launches": K * bench.launches_per_step,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
+    if rank == 0 and args.all_workloads:
+        line["workloads"] = other_workloads(args, device, stream, peak)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def other_workloads(args, device, stream, peak):
+    out = {}
+    for name in workloads.WORKLOADS:
+        if name == args.workload:
+            continue
+        b = Bench(name, args.seed, device, 0)
+        b.check_budget()
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                b.step(i, stream)
+        torch.cuda.synchronize()
+        K = 200 if not b.has_state else 40
+        ms, _ = timed_graph_run(b, K, stream, 1)
+        ms_v, _ = timed_graph_run(b, K, stream, 1, commit=False)
+        v_us = ms_v * 1e3 / K
+        entry = {"rows_per_s": b.rows_per_step * K / (ms * 1e-3), "ms_per_step": ms / K,
+                 "verify_us": v_us, "verify_gbs": b.verify_bytes / (v_us * 1e-6) / 1e9,
+                 "verify_frac": b.verify_bytes / (v_us * 1e-6) / 1e9 / peak,
+                 "verify_algorithmic_bytes": b.verify_bytes, "rows_per_step": b.rows_per_step}
+        if b.has_state:
+            ms_c, _ = timed_graph_run(b, K, stream, 1, verify=False)
+            c_us = ms_c * 1e3 / K
+            entry.update({"commit_us": c_us, "commit_gbs": b.commit_bytes / (c_us * 1e-6) / 1e9,
+                          "commit_frac": b.commit_bytes / (c_us * 1e-6) / 1e9 / peak,
+                          "commit_algorithmic_bytes": b.commit_bytes})
+        out[name] = entry
+        del b
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    r = workloads.make_round(args.workload, seed=args.seed, device="cpu")
+    off = r.row_offsets.numpy()
+    target = (oracle.decode_bf16(r.target.view(torch.int16).numpy().view(np.uint16))
+              if r.target.dtype == torch.bfloat16 else r.target.numpy().astype(np.float64))
+    draft = (oracle.decode_bf16(r.draft.view(torch.int16).numpy().view(np.uint16))
+             if r.draft is not None else None)
+    # Each step: a bounded sample of the round (whole lanes), sized to ~0.5 s.
+    t0 = time.time()
+    oracle.verify_round(target, draft, r.draft_tokens.numpy(), r.draft_lens.numpy()[:1], off[:2],
+                        r.temperatures.numpy()[:1], seed=r.seed)
+    per_lane = max(time.time() - t0, 1e-4)
+    take = int(max(1, min(r.lanes, 0.5 / per_lane)))
+    rows_per_step = int(off[take])
+
+    def step():
+        return oracle.verify_round(target, draft, r.draft_tokens.numpy(), r.draft_lens.numpy()[:take],
+                                   off[:take + 1], r.temperatures.numpy()[:take], seed=r.seed)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.time()
+    for _ in range(args.steps):
+        step()
+    dt = time.time() - t0
+    value = rows_per_step * args.steps / dt
+    sample = f"{take} of {r.lanes} lanes ({rows_per_step} rows) per step"
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "lanes": r.lanes, "vocab": r.vocab,
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=workloads.WORKLOADS, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--only", dest="all_workloads", action="store_false",
+                    help="measure only --workload (by default the other workloads are measured "
+                         "too and reported under 'workloads')")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,282 @@
+"""Python binding of libspecverify, the GB300 verify-round library.
+
+Argument marshalling only: every step of the verify round runs in the CUDA
+kernels behind the C ABI of ``include/spec_verify.h``.  Tensors must already be
+on the GPU; PyTorch provides device memory and the current stream.  If the
+shared library has not been built every entry point raises -- there is no CPU
+fallback.
+"""
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH, build_library
+
+__all__ = [
+    "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
+    "SPEC_ERR_NONFINITE", "SPEC_ERR_TOKEN_RANGE", "SPEC_ERR_LAYOUT", "SPEC_ERR_TIMEOUT",
+    "SPEC_MAX_DRAFTS", "SpecError", "ROW_STATS_FIELDS", "load_library", "build_library",
+    "spec_row_budget", "spec_verify_accept", "spec_commit_state", "spec_status_string",
+    "spec_verify_launch_shape", "spec_round_uniforms", "new_row_stats", "row_stats_view",
+]
+
+SPEC_OK = 0
+SPEC_ERR_INVALID_ARG = 1
+SPEC_ERR_UNSUPPORTED = 2
+SPEC_ERR_CUDA = 3
+SPEC_ERR_NONFINITE = 4
+SPEC_ERR_TOKEN_RANGE = 5
+SPEC_ERR_LAYOUT = 6
+SPEC_ERR_TIMEOUT = 7
+SPEC_MAX_DRAFTS = 15
+
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+# spec_row_stats: 8 x 32-bit words per row.
+ROW_STATS_FIELDS = ("argmax", "max_logit", "lse", "logp_d", "logq_d", "resid_mass", "drawn", "flags")
+_ROW_STATS_INT = {"argmax", "drawn", "flags"}
+
+
+class SpecError(RuntimeError):
+    """A non-zero status returned by the library."""
+
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__(f"{what}: {spec_status_string(code)} ({code})")
+
+
+class _Args(ctypes.Structure):
+    _fields_ = [
+        ("target_logits", ctypes.c_void_p),
+        ("draft_logits", ctypes.c_void_p),
+        ("dtype", ctypes.c_int),
+        ("ld", ctypes.c_int64),
+        ("V", ctypes.c_int32),
+        ("lanes", ctypes.c_int32),
+        ("rows", ctypes.c_int32),
+        ("draft_tokens", ctypes.c_void_p),
+        ("draft_lens", ctypes.c_void_p),
+        ("row_offsets", ctypes.c_void_p),
+        ("temperatures", ctypes.c_void_p),
+        ("seed", ctypes.c_uint64),
+        ("committed", ctypes.c_void_p),
+        ("out_tokens", ctypes.c_void_p),
+        ("lane_status", ctypes.c_void_p),
+        ("row_stats", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def load_library():
+    """Load libspecverify.so (built in-tree); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; call speculative_decoding_verify_bf16_gb300."
+                           "build_library() (needs nvcc) -- there is no CPU fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.spec_row_budget.restype = ctypes.c_int32
+    lib.spec_row_budget.argtypes = [ctypes.c_int32] * 3
+    lib.spec_verify_accept.restype = ctypes.c_int
+    lib.spec_verify_accept.argtypes = [ctypes.POINTER(_Args), ctypes.c_void_p]
+    lib.spec_commit_state.restype = ctypes.c_int
+    lib.spec_commit_state.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64,
+                                      ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                      ctypes.c_void_p, ctypes.c_void_p]
+    lib.spec_status_string.restype = ctypes.c_char_p
+    lib.spec_status_string.argtypes = [ctypes.c_int]
+    lib.spec_round_uniforms.restype = ctypes.c_int
+    lib.spec_round_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_void_p, ctypes.c_void_p]
+    lib.spec_verify_launch_shape.restype = ctypes.c_int
+    lib.spec_verify_launch_shape.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int] + \
+        [ctypes.POINTER(ctypes.c_int32)] * 4
+    _lib = lib
+    return lib
+
+
+def spec_status_string(code):
+    return load_library().spec_status_string(int(code)).decode()
+
+
+def spec_row_budget(draft_tokens, row_budget, lanes):
+    """Drafts per lane under a row budget; raises ValueError on bad arguments."""
+    r = load_library().spec_row_budget(int(draft_tokens), int(row_budget), int(lanes))
+    if r < 0:
+        raise ValueError(f"spec_row_budget({draft_tokens}, {row_budget}, {lanes}): "
+                         f"{spec_status_string(-r)}")
+    return int(r)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, device, numel=None):
+    if not isinstance(t, torch.Tensor) or t.device != device:
+        raise ValueError(f"{name} must be a tensor on {device}")
+    if t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} needs at least {numel} elements")
+
+
+def new_row_stats(rows, device):
+    """An int32 [rows, 8] buffer laid out as spec_row_stats."""
+    return torch.empty(rows, 8, dtype=torch.int32, device=device)
+
+
+def row_stats_view(buf):
+    """Dict of named columns of a row-stats buffer (float fields viewed as float32)."""
+    out = {}
+    for i, name in enumerate(ROW_STATS_FIELDS):
+        col = buf[:, i].contiguous()
+        out[name] = col if name in _ROW_STATS_INT else col.view(torch.float32)
+    return out
+
+
+def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, temperatures, seed,
+                       committed, out_tokens, lane_status=None, row_stats=None, stream=None,
+                       rows=None):
+    """Launch the fused verify kernel (see spec_verify_accept in include/spec_verify.h).
+
+    target, draft: [rows, >= V] bf16 or float32 CUDA tensors with unit inner
+    stride (draft may be None when no lane samples); the row stride is taken as
+    ld.  draft_tokens, out_tokens: int32 [rows]; draft_lens, committed,
+    lane_status: int32 [lanes]; row_offsets: int32 [lanes + 1]; temperatures:
+    float32 [lanes]; row_stats: int32 [rows, 8] from new_row_stats().
+    ``rows`` defaults to target.shape[0] (it must equal row_offsets[-1]).
+    """
+    lib = load_library()
+    if target.dim() != 2 or target.stride(1) != 1 or target.dtype not in _DTYPES:
+        raise ValueError("target must be a 2-D bf16/float32 tensor with unit inner stride")
+    dev = target.device
+    if dev.type != "cuda":
+        raise ValueError("target must be on a CUDA device")
+    if draft is not None and (draft.dtype != target.dtype or draft.device != dev or draft.dim() != 2
+                              or draft.stride(1) != 1 or draft.stride(0) != target.stride(0)):
+        raise ValueError("draft must match target's dtype, device and row stride")
+    lanes = draft_lens.numel()
+    nrows = target.shape[0] if rows is None else int(rows)
+    if nrows > target.shape[0] or (draft is not None and nrows > draft.shape[0]):
+        raise ValueError("rows exceeds the rows of the logits tensors")
+    _need(draft_tokens, "draft_tokens", torch.int32, dev, nrows)
+    _need(draft_lens, "draft_lens", torch.int32, dev)
+    _need(row_offsets, "row_offsets", torch.int32, dev, lanes + 1)
+    _need(temperatures, "temperatures", torch.float32, dev, lanes)
+    _need(committed, "committed", torch.int32, dev, lanes)
+    _need(out_tokens, "out_tokens", torch.int32, dev, nrows)
+    if lane_status is not None:
+        _need(lane_status, "lane_status", torch.int32, dev, lanes)
+    if row_stats is not None:
+        _need(row_stats, "row_stats", torch.int32, dev, nrows * 8)
+    a = _Args(
+        target_logits=target.data_ptr(),
+        draft_logits=None if draft is None else draft.data_ptr(),
+        dtype=_DTYPES[target.dtype],
+        ld=target.stride(0),
+        V=target.shape[1],
+        lanes=lanes,
+        rows=nrows,
+        draft_tokens=draft_tokens.data_ptr(),
+        draft_lens=draft_lens.data_ptr(),
+        row_offsets=row_offsets.data_ptr(),
+        temperatures=temperatures.data_ptr(),
+        seed=int(seed) & ((1 << 64) - 1),
+        committed=committed.data_ptr(),
+        out_tokens=out_tokens.data_ptr(),
+        lane_status=None if lane_status is None else lane_status.data_ptr(),
+        row_stats=None if row_stats is None else row_stats.data_ptr(),
+    )
+    code = lib.spec_verify_accept(ctypes.byref(a), _stream(stream))
+    if code != SPEC_OK:
+        raise SpecError(code, "spec_verify_accept")
+
+
+def spec_verify_accept_raw(args, stream):
+    """Call spec_verify_accept with a prepared _Args (no checks); returns the status."""
+    return load_library().spec_verify_accept(ctypes.byref(args), stream)
+
+
+def make_args(target, draft, draft_tokens, draft_lens, row_offsets, temperatures, seed,
+              committed, out_tokens, lane_status=None, row_stats=None, V=None, rows=None):
+    """Build the C argument struct once (for tight loops that call it repeatedly)."""
+    return _Args(
+        target_logits=target.data_ptr(),
+        draft_logits=None if draft is None else draft.data_ptr(),
+        dtype=_DTYPES[target.dtype],
+        ld=target.stride(0),
+        V=target.shape[1] if V is None else int(V),
+        lanes=draft_lens.numel(),
+        rows=target.shape[0] if rows is None else int(rows),
+        draft_tokens=draft_tokens.data_ptr(),
+        draft_lens=draft_lens.data_ptr(),
+        row_offsets=row_offsets.data_ptr(),
+        temperatures=temperatures.data_ptr(),
+        seed=int(seed) & ((1 << 64) - 1),
+        committed=committed.data_ptr(),
+        out_tokens=out_tokens.data_ptr(),
+        lane_status=None if lane_status is None else lane_status.data_ptr(),
+        row_stats=None if row_stats is None else row_stats.data_ptr(),
+    )
+
+
+def spec_commit_state(staged, live, committed, lane_status=None, stream=None):
+    """Copy staged[b, committed[b] - 1] into live[b] for every lane (on the GPU).
+
+    staged: [lanes, cols, ...] and live: [lanes, ...] CUDA tensors of one dtype
+    whose per-column snapshot is contiguous.
+    """
+    lib = load_library()
+    lanes, cols = staged.shape[0], staged.shape[1]
+    dev = staged.device
+    if live.device != dev or live.dtype != staged.dtype or live.shape[0] != lanes:
+        raise ValueError("live must match staged's device, dtype and lane count")
+    if not staged[0, 0].is_contiguous() or not live[0].is_contiguous():
+        raise ValueError("each snapshot must be contiguous")
+    esize = staged.element_size()
+    bytes_per_col = live[0].numel() * esize
+    if staged[0, 0].numel() * esize != bytes_per_col:
+        raise ValueError("staged and live snapshots differ in size")
+    _need(committed, "committed", torch.int32, dev, lanes)
+    if lane_status is not None:
+        _need(lane_status, "lane_status", torch.int32, dev, lanes)
+    code = lib.spec_commit_state(
+        _ptr(staged), _ptr(live), _ptr(committed), lanes, cols, bytes_per_col,
+        staged.stride(0) * esize, staged.stride(1) * esize, live.stride(0) * esize,
+        _ptr(lane_status), _stream(stream))
+    if code != SPEC_OK:
+        raise SpecError(code, "spec_commit_state")
+
+
+def spec_round_uniforms(seed, lanes, positions, device=None, stream=None):
+    """float32 [lanes, positions, 2]: the (u, u') pairs the verify kernel draws."""
+    lib = load_library()
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    out = torch.empty(lanes, positions, 2, dtype=torch.float32, device=device)
+    code = lib.spec_round_uniforms(int(seed) & ((1 << 64) - 1), int(lanes), int(positions),
+                                   _ptr(out), _stream(stream))
+    if code != SPEC_OK:
+        raise SpecError(code, "spec_round_uniforms")
+    return out
+
+
+def spec_verify_launch_shape(lanes, V, dtype=torch.bfloat16):
+    lib = load_library()
+    vals = [ctypes.c_int32() for _ in range(4)]
+    code = lib.spec_verify_launch_shape(int(lanes), int(V), _DTYPES[dtype], *[ctypes.byref(v) for v in vals])
+    if code != SPEC_OK:
+        raise SpecError(code, "spec_verify_launch_shape")
+    return dict(zip(("cluster_ctas", "threads", "slice", "smem_bytes"), (v.value for v in vals)))

@@ -1,0 +1,393 @@
+// spec_verify.cu -- host side of the C ABI declared in include/spec_verify.h:
+// argument checks, launch-shape selection and kernel launches.  The library
+// allocates no device memory; it caches per-device kernel attributes only.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "commit_kernel.cuh"
+#include "spec_verify.h"
+#include "verify_kernel.cuh"
+
+namespace {
+
+using specv::bf16_tag;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceCache {
+  bool ready = false;
+  int sms = 0;
+  int smem_optin = 0;
+  bool verify_attr[4] = {false, false, false, false};  // per kernel instantiation
+  bool commit_attr = false;
+};
+
+std::mutex g_mutex;
+DeviceCache g_cache[kMaxDevices];
+
+int env_int(const char* name, int fallback) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || *v == '\0') return fallback;
+  return std::atoi(v);
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+int device_cache(DeviceCache** out, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceCache& c = g_cache[dev];
+  if (!c.ready) {
+    if (cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+      return SPEC_ERR_CUDA;
+    c.ready = true;
+  }
+  *out = &c;
+  if (dev_out) *dev_out = dev;
+  return SPEC_OK;
+}
+
+struct VerifyShape {
+  int cluster;
+  int slice;
+  int slot_bytes;
+  int nslots;
+  int head_bytes;
+  int smem;
+};
+
+// One cluster of `cluster` CTAs per lane; each CTA reduces `slice` elements of
+// every row of its lane.  Enough CTAs to fill the GPU about twice over, but
+// no fewer than 2048 elements per CTA.  The ring holds whole slices when they
+// fit in a 32 KB slot.
+VerifyShape choose_shape(int lanes, int V, int esize, bool aligned, int sms, int force_cluster) {
+  VerifyShape s{};
+  const int vec = 16 / esize;
+  int C = force_cluster > 0 ? force_cluster : env_int("SPEC_VERIFY_CLUSTER", 0);
+  if (C <= 0) {
+    C = 1;
+    while (C < specv::kMaxCluster && static_cast<int64_t>(lanes) * C < 2LL * sms) C *= 2;
+    while (C > 1 && (V + C - 1) / C < 2048) C /= 2;
+  }
+  if (C > specv::kMaxCluster) C = specv::kMaxCluster;
+  s.cluster = C;
+  s.slice = static_cast<int>(round_up((V + C - 1) / C, vec));
+  s.head_bytes = static_cast<int>(round_up(sizeof(specv::SmemHead), 128));
+  if (!aligned) {
+    s.slot_bytes = 16;
+    s.nslots = 0;
+    s.smem = s.head_bytes;
+    return s;
+  }
+  const int64_t slice_bytes = static_cast<int64_t>(s.slice) * esize;
+  const int64_t slot_max = static_cast<int64_t>(env_int("SPEC_VERIFY_SLOT_KB", 32)) * 1024;
+  const int64_t chunks = (slice_bytes + slot_max - 1) / slot_max;
+  s.slot_bytes = static_cast<int>(round_up((slice_bytes + chunks - 1) / chunks, 16));
+  const bool many = static_cast<int64_t>(lanes) * C > sms;
+  const int64_t ring = static_cast<int64_t>(env_int("SPEC_VERIFY_RING_KB", many ? 96 : 160)) * 1024;
+  int nslots = static_cast<int>(ring / s.slot_bytes);
+  if (nslots < 2) nslots = 2;
+  if (nslots > specv::kMaxSlots) nslots = specv::kMaxSlots;
+  s.nslots = nslots;
+  s.smem = s.head_bytes + nslots * s.slot_bytes;
+  return s;
+}
+
+template <typename T, bool ALIGNED>
+void* verify_kernel_ptr() {
+  return reinterpret_cast<void*>(&specv::verify_accept_kernel<T, ALIGNED>);
+}
+
+int kernel_index(int dtype, bool aligned) { return dtype * 2 + (aligned ? 1 : 0); }
+
+void* pick_verify_kernel(int dtype, bool aligned) {
+  if (dtype == SPEC_BF16) return aligned ? verify_kernel_ptr<bf16_tag, true>() : verify_kernel_ptr<bf16_tag, false>();
+  return aligned ? verify_kernel_ptr<float, true>() : verify_kernel_ptr<float, false>();
+}
+
+bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Cluster sizes already found schedulable, per device / kernel / shared memory.
+struct ClusterFit {
+  int dev;
+  void* kernel;
+  int smem;
+  int cluster;
+  int fits;
+};
+constexpr int kFitCache = 64;
+ClusterFit g_fit[kFitCache];
+int g_fit_n = 0;
+
+// True if at least one cluster of `cluster` CTAs with `smem` bytes each can be
+// resident at once on this device.
+bool cluster_fits(int dev, void* kernel, int cluster, int smem) {
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (int i = 0; i < g_fit_n; ++i)
+      if (g_fit[i].dev == dev && g_fit[i].kernel == kernel && g_fit[i].smem == smem &&
+          g_fit[i].cluster == cluster)
+        return g_fit[i].fits != 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
+  cfg.blockDim = dim3(specv::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const bool ok = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n > 0;
+  if (!ok) cudaGetLastError();
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_fit_n < kFitCache) g_fit[g_fit_n++] = ClusterFit{dev, kernel, smem, cluster, ok ? 1 : 0};
+  return ok;
+}
+
+__global__ void round_uniforms_kernel(uint64_t seed, int32_t lanes, int32_t positions, float* out) {
+  const int64_t total = static_cast<int64_t>(lanes) * positions;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int b = static_cast<int>(i / positions), j = static_cast<int>(i % positions);
+    const float2 u = specv::round_uniforms(seed, b, j);
+    out[2 * i] = u.x;
+    out[2 * i + 1] = u.y;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_round_uniforms(uint64_t seed, int32_t lanes, int32_t positions, float* out, void* stream) {
+  if (lanes < 0 || positions < 0) return SPEC_ERR_INVALID_ARG;
+  const int64_t total = static_cast<int64_t>(lanes) * positions;
+  if (total == 0) return SPEC_OK;
+  if (out == nullptr) return SPEC_ERR_INVALID_ARG;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  round_uniforms_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      seed, lanes, positions, out);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+
+int32_t spec_row_budget(int32_t draft_tokens, int32_t row_budget, int32_t lanes) {
+  if (lanes <= 0 || draft_tokens < 0 || row_budget < 0) return -SPEC_ERR_INVALID_ARG;
+  const int32_t rows = (row_budget == 0) ? 8 : row_budget;
+  int32_t per_lane = rows / lanes - 1;
+  if (per_lane > draft_tokens) per_lane = draft_tokens;
+  return per_lane < 0 ? 0 : per_lane;
+}
+
+const char* spec_status_string(int status) {
+  switch (status) {
+    case SPEC_OK: return "SPEC_OK";
+    case SPEC_ERR_INVALID_ARG: return "SPEC_ERR_INVALID_ARG";
+    case SPEC_ERR_UNSUPPORTED: return "SPEC_ERR_UNSUPPORTED";
+    case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA";
+    case SPEC_ERR_NONFINITE: return "SPEC_ERR_NONFINITE";
+    case SPEC_ERR_TOKEN_RANGE: return "SPEC_ERR_TOKEN_RANGE";
+    case SPEC_ERR_LAYOUT: return "SPEC_ERR_LAYOUT";
+    case SPEC_ERR_TIMEOUT: return "SPEC_ERR_TIMEOUT";
+    default: return "SPEC_ERR_UNKNOWN";
+  }
+}
+
+int spec_verify_launch_shape(int32_t lanes, int32_t V, spec_dtype dtype, int32_t* cluster_ctas,
+                             int32_t* threads, int32_t* slice, int32_t* smem_bytes) {
+  if (lanes <= 0 || V <= 0 || (dtype != SPEC_F32 && dtype != SPEC_BF16)) return SPEC_ERR_INVALID_ARG;
+  DeviceCache* dc = nullptr;
+  if (device_cache(&dc, nullptr) != SPEC_OK) return SPEC_ERR_CUDA;
+  const VerifyShape s = choose_shape(lanes, V, dtype == SPEC_BF16 ? 2 : 4, true, dc->sms, 0);
+  if (cluster_ctas) *cluster_ctas = s.cluster;
+  if (threads) *threads = specv::kThreads;
+  if (slice) *slice = s.slice;
+  if (smem_bytes) *smem_bytes = s.smem;
+  return SPEC_OK;
+}
+
+int spec_verify_accept(const spec_verify_args* a, void* stream) {
+  if (a == nullptr) return SPEC_ERR_INVALID_ARG;
+  if (a->target_logits == nullptr || a->draft_tokens == nullptr || a->draft_lens == nullptr ||
+      a->row_offsets == nullptr || a->temperatures == nullptr || a->committed == nullptr ||
+      a->out_tokens == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  if (a->V <= 0 || a->lanes <= 0 || a->rows < a->lanes || a->ld < a->V) return SPEC_ERR_INVALID_ARG;
+  if (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(a->lanes) * specv::kMaxCluster > INT32_MAX) return SPEC_ERR_INVALID_ARG;
+
+  DeviceCache* dc = nullptr;
+  int dev = 0;
+  if (device_cache(&dc, &dev) != SPEC_OK) return SPEC_ERR_CUDA;
+
+  const int esize = (a->dtype == SPEC_BF16) ? 2 : 4;
+  const bool aligned = is_aligned16(a->target_logits) &&
+                       (a->draft_logits == nullptr || is_aligned16(a->draft_logits)) &&
+                       ((a->ld * esize) % 16 == 0);
+  VerifyShape s = choose_shape(a->lanes, a->V, esize, aligned, dc->sms, 0);
+  if (s.smem > dc->smem_optin) return SPEC_ERR_UNSUPPORTED;
+
+  void* kernel = pick_verify_kernel(a->dtype, aligned);
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    bool& done = dc->verify_attr[kernel_index(a->dtype, aligned)];
+    if (!done) {
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dc->smem_optin) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+      done = true;
+    }
+  }
+  // A cluster must fit into one GPU processing cluster; shrink it until one does.
+  while (s.cluster > 1 && !cluster_fits(dev, kernel, s.cluster, s.smem))
+    s = choose_shape(a->lanes, a->V, esize, aligned, dc->sms, s.cluster / 2);
+
+  specv::VerifyParams p{};
+  p.target = static_cast<const uint8_t*>(a->target_logits);
+  p.draft = static_cast<const uint8_t*>(a->draft_logits);
+  p.ld_bytes = a->ld * esize;
+  p.V = a->V;
+  p.lanes = a->lanes;
+  p.rows = a->rows;
+  p.draft_tokens = a->draft_tokens;
+  p.draft_lens = a->draft_lens;
+  p.row_offsets = a->row_offsets;
+  p.temps = a->temperatures;
+  p.seed = a->seed;
+  p.committed = a->committed;
+  p.out_tokens = a->out_tokens;
+  p.lane_status = a->lane_status;
+  p.row_stats = a->row_stats;
+  p.cluster = s.cluster;
+  p.slice = s.slice;
+  p.slot_bytes = s.slot_bytes;
+  p.nslots = s.nslots;
+  p.head_bytes = s.head_bytes;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(s.cluster * a->lanes), 1, 1);
+  cfg.blockDim = dim3(specv::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(s.smem);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = static_cast<unsigned>(s.cluster);
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  void* kargs[] = {&p};
+  if (cudaLaunchKernelExC(&cfg, kernel, kargs) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
+}
+
+int spec_commit_state(const void* staged, void* live, const int32_t* committed, int32_t lanes,
+                      int32_t cols, uint64_t bytes_per_col, uint64_t staged_lane_stride,
+                      uint64_t staged_col_stride, uint64_t live_lane_stride, int32_t* lane_status,
+                      void* stream) {
+  if (lanes < 0 || cols <= 0) return SPEC_ERR_INVALID_ARG;
+  if (lanes == 0 || bytes_per_col == 0) return SPEC_OK;
+  if (staged == nullptr || live == nullptr || committed == nullptr) return SPEC_ERR_INVALID_ARG;
+  if (bytes_per_col > staged_col_stride && cols > 1) return SPEC_ERR_INVALID_ARG;
+  if (lanes > 1 && (bytes_per_col > live_lane_stride ||
+                    static_cast<uint64_t>(cols - 1) * staged_col_stride + bytes_per_col > staged_lane_stride))
+    return SPEC_ERR_INVALID_ARG;
+
+  DeviceCache* dc = nullptr;
+  if (device_cache(&dc, nullptr) != SPEC_OK) return SPEC_ERR_CUDA;
+
+  specv::CommitParams p{};
+  p.staged = static_cast<const uint8_t*>(staged);
+  p.live = static_cast<uint8_t*>(live);
+  p.committed = committed;
+  p.lane_status = lane_status;
+  p.lanes = lanes;
+  p.cols = cols;
+  p.bytes_per_col = bytes_per_col;
+  p.staged_lane_stride = staged_lane_stride;
+  p.staged_col_stride = staged_col_stride;
+  p.live_lane_stride = live_lane_stride;
+
+  const bool aligned = is_aligned16(staged) && is_aligned16(live) && bytes_per_col % 16 == 0 &&
+                       staged_lane_stride % 16 == 0 && staged_col_stride % 16 == 0 &&
+                       live_lane_stride % 16 == 0;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  void* kargs[] = {&p};
+  void* kernel = nullptr;
+
+  if (aligned) {
+    int chunk = env_int("SPEC_COMMIT_CHUNK_KB", 32) * 1024;
+    int nbuf = env_int("SPEC_COMMIT_NBUF", 6);
+    int per_sm = env_int("SPEC_COMMIT_CTAS_PER_SM", 1);
+    if (nbuf < 2) nbuf = 2;
+    if (nbuf > specv::kCommitMaxBufs) nbuf = specv::kCommitMaxBufs;
+    if (per_sm < 1) per_sm = 1;
+    if (static_cast<uint64_t>(chunk) > bytes_per_col) chunk = static_cast<int>(bytes_per_col);
+    while (specv::kCommitHead + static_cast<int64_t>(nbuf) * chunk > dc->smem_optin && nbuf > 2) --nbuf;
+    while (specv::kCommitHead + static_cast<int64_t>(nbuf) * chunk > dc->smem_optin) chunk /= 2;
+    chunk = static_cast<int>(chunk / 16 * 16);
+    if (chunk < 16) chunk = 16;
+    p.chunk_bytes = static_cast<uint32_t>(chunk);
+    p.chunks_per_lane = (bytes_per_col + chunk - 1) / chunk;
+    p.total_items = p.chunks_per_lane * static_cast<uint64_t>(lanes);
+    p.nbuf = nbuf;
+    uint64_t grid = static_cast<uint64_t>(dc->sms) * per_sm;
+    if (grid > p.total_items) grid = p.total_items;
+    kernel = reinterpret_cast<void*>(&specv::commit_bulk_kernel);
+    const int smem = specv::kCommitHead + nbuf * chunk;
+    {
+      std::lock_guard<std::mutex> lock(g_mutex);
+      if (!dc->commit_attr) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dc->smem_optin) !=
+            cudaSuccess)
+          return SPEC_ERR_CUDA;
+        dc->commit_attr = true;
+      }
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(specv::kCommitThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  } else {
+    kernel = reinterpret_cast<void*>(&specv::commit_bytes_kernel);
+    const uint64_t total = static_cast<uint64_t>(lanes) * bytes_per_col;
+    uint64_t grid = (total + 255) / 256;
+    const uint64_t cap = static_cast<uint64_t>(dc->sms) * 8;
+    if (grid > cap) grid = cap;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+  }
+  if (cudaLaunchKernelExC(&cfg, kernel, kargs) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+"""The C-ABI library loads and exports what include/*.h declares (no GPU needed)."""
+
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT, read_golden
+
+import speculative_decoding_verify_bf16_gb300 as sv
+
+
+def _declared_functions():
+    names = set()
+    for path in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \t\*]*?\b(spec_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sv.build_library()
+    return sv.load_library()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for want in ["spec_row_budget", "spec_verify_accept", "spec_commit_state",
+                 "spec_status_string", "spec_verify_launch_shape", "spec_round_uniforms"]:
+        assert want in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", sv.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in _declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_row_budget_worked_example_through_the_abi(lib):
+    for draft_tokens, budget, lanes, expected in read_golden("row_budget_worked_example.txt"):
+        assert sv.spec_row_budget(draft_tokens, budget, lanes) == expected
+
+
+def test_row_budget_errors_through_the_abi(lib):
+    for args in [(3, 8, 0), (3, 8, -2), (-1, 8, 1), (3, -1, 1)]:
+        assert lib.spec_row_budget(*args) == -sv.SPEC_ERR_INVALID_ARG
+        with pytest.raises(ValueError):
+            sv.spec_row_budget(*args)
+    assert sv.spec_row_budget(7, 1024, 128) == 7
+
+
+def test_status_strings(lib):
+    names = ["SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
+             "SPEC_ERR_NONFINITE", "SPEC_ERR_TOKEN_RANGE", "SPEC_ERR_LAYOUT", "SPEC_ERR_TIMEOUT"]
+    for code, name in enumerate(names):
+        assert sv.spec_status_string(code) == name
+    assert sv.spec_status_string(99) == "SPEC_ERR_UNKNOWN"
+
+
+def test_calls_with_bad_arguments_fail_on_the_host(lib):
+    # NULL argument struct and NULL out pointer: rejected before touching a GPU.
+    assert lib.spec_verify_accept(None, None) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_round_uniforms(1, 4, 4, None, None) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_commit_state(None, None, None, -1, 1, 16, 16, 16, 16, None, None) == \
+        sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_commit_state(None, None, None, 0, 1, 16, 16, 16, 16, None, None) == sv.SPEC_OK

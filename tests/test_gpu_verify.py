@@ -1,0 +1,267 @@
+"""GPU parity: the fused verify kernel against the CPU oracle, through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import speculative_decoding_verify_bf16_gb300 as sv
+from gpu_harness import compare, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    sv.build_library()
+    sv.load_library()
+
+
+# V spans tiny vocabularies (one CTA, ragged tails shorter than a vector),
+# several slices per lane, and a vocabulary that does not divide into vectors.
+SMALL_CASES = [
+    # (vocab, kmax, lanes, dtype, sampled, fixed_k, seed)
+    (1, 3, 3, "bf16", "none", False, 1),
+    (7, 4, 3, "bf16", "mixed", False, 2),
+    (8, 7, 17, "bf16", "mixed", False, 3),
+    (9, 2, 5, "f32", "mixed", False, 4),
+    (1023, 7, 17, "bf16", "all", False, 5),
+    (4097, 5, 3, "f32", "all", False, 6),
+    (4097, 15, 2, "bf16", "mixed", True, 7),
+    (40000, 7, 9, "bf16", "mixed", False, 8),
+    (65537, 3, 1, "bf16", "all", True, 9),
+    (151936, 7, 3, "bf16", "mixed", False, 10),
+    (262144, 2, 2, "bf16", "all", True, 11),
+    (32000, 0, 6, "bf16", "mixed", True, 12),
+    (5000, 7, 33, "f32", "none", False, 13),
+]
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: f"V{c[0]}-k{c[1]}-B{c[2]}-{c[3]}-{c[4]}")
+def test_small_shapes_match_oracle(case):
+    vocab, kmax, lanes, dtype, sampled, fixed_k, seed = case
+    r = workloads.make_custom_round(seed, DEV, lanes=lanes, vocab=vocab, kmax=kmax, dtype=dtype,
+                                    sampled=sampled, fixed_k=fixed_k)
+    gpu = run_gpu(r)
+    orc = run_oracle(r)
+    compare(r, gpu, orc)
+
+
+@pytest.mark.parametrize("ld_extra", [8, 5, 64])
+def test_padded_rows_match_oracle(ld_extra):
+    """Row stride ld > V: padding (huge values) must never be read.
+
+    ld_extra = 5 makes rows misaligned, which takes the element-wise path.
+    """
+    vocab = 3001
+    r = workloads.make_custom_round(21, DEV, lanes=7, vocab=vocab, kmax=5, dtype="bf16",
+                                    sampled="mixed", ld=vocab + ld_extra)
+    assert r.target.stride(0) == vocab + ld_extra
+    compare(r, run_gpu(r), run_oracle(r))
+
+
+def test_misaligned_base_takes_elementwise_path():
+    vocab = 20000
+    r = workloads.make_custom_round(22, DEV, lanes=5, vocab=vocab, kmax=4, dtype="bf16", sampled="mixed")
+    # shift both logits arrays by one element: base addresses no longer 16-byte aligned
+    for name in ("target", "draft"):
+        t = getattr(r, name)
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+        buf[1:] = t.reshape(-1)
+        setattr(r, name, buf[1:].view(t.shape))
+    assert r.target.data_ptr() % 16 != 0
+    compare(r, run_gpu(r), run_oracle(r))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_many_seeds_mixed(seed):
+    r = workloads.make_custom_round(100 + seed, DEV, lanes=64, vocab=12000, kmax=7, dtype="bf16",
+                                    sampled="mixed")
+    compare(r, run_gpu(r), run_oracle(r))
+
+
+@pytest.mark.parametrize("name", workloads.WORKLOADS)
+def test_named_workloads_full_size(name):
+    """Every workload at its full size, in the launch configuration the bench uses."""
+    r = workloads.make_round(name, seed=7, device=DEV)
+    if name == workloads.RAGGED_MIXED_B128:
+        assert sv.spec_row_budget(workloads.RAGGED_DRAFT_TOKENS, workloads.RAGGED_ROW_BUDGET,
+                                  r.lanes) == workloads.RAGGED_DRAFT_TOKENS
+        assert r.rows <= workloads.RAGGED_ROW_BUDGET
+    gpu = run_gpu(r)
+    orc = run_oracle(r)
+    compare(r, gpu, orc)
+    assert (gpu["committed"] >= 1).all()
+    assert (gpu["committed"] <= r.draft_lens.cpu().numpy() + 1).all()
+
+
+def test_round_uniforms_match_the_oracle_generator():
+    seed = 0x0123456789ABCDEF
+    u = sv.spec_round_uniforms(seed, 40, 16).cpu().numpy()
+    for b in range(40):
+        for j in range(16):
+            ua, us = oracle.round_uniforms(seed, b, j)
+            assert u[b, j, 0] == ua and u[b, j, 1] == us, (b, j)
+    # large lane ids and seeds exercise the high counter and key words
+    u = sv.spec_round_uniforms(2 ** 64 - 1, 3, 2).cpu().numpy()
+    assert u[2, 1, 0] == oracle.round_uniforms(2 ** 64 - 1, 2, 1)[0]
+
+
+def test_greedy_equals_plain_argmax_decode_on_the_gpu():
+    """Rounds through the GPU kernel emit the plain argmax stream of a toy model."""
+    from oracle_checks import ToyLM
+
+    vocab, k = 300, 5
+    lm = ToyLM(vocab, seed=13)
+    context = [1, 2]
+    plain = [lm.next_token(context)]
+    while len(plain) < 80:
+        plain.append(lm.next_token(context + plain))
+    rng = np.random.default_rng(1)
+    consumed, anchor, emitted = list(context), plain[0], [plain[0]]
+    while len(emitted) < 60:
+        pos = len(emitted) - 1
+        drafts = [plain[pos + 1 + i] if rng.random() < 0.7 else int(rng.integers(vocab)) for i in range(k)]
+        cols = [anchor] + drafts
+        rows = np.stack([lm.logits(consumed + cols[:j + 1]) for j in range(k + 1)])
+        target = torch.tensor(rows, dtype=torch.float32, device=DEV)
+        r = workloads.RoundInputs("toy", vocab, 1, k + 1, "f32", target, None,
+                                  torch.tensor(drafts + [-1], dtype=torch.int32, device=DEV),
+                                  torch.tensor([k], dtype=torch.int32, device=DEV),
+                                  torch.tensor([0, k + 1], dtype=torch.int32, device=DEV),
+                                  torch.zeros(1, dtype=torch.float32, device=DEV), 0)
+        g = run_gpu(r)
+        c = int(g["committed"][0])
+        toks = g["out_tokens"][:c].tolist()
+        consumed += cols[:c]
+        anchor = toks[-1]
+        emitted += toks
+    assert emitted[:60] == plain[:60]
+
+
+def test_sampled_marginals_on_the_gpu():
+    """Emitted tokens follow p: chi-square over many lanes sharing one set of rows."""
+    from scipy import stats
+
+    rng = np.random.default_rng(5)
+    vocab, k, temp, lanes = 6, 2, 0.9, 40000
+    t_rows = rng.normal(size=(k + 1, vocab)) * 1.2
+    d_rows = t_rows + rng.normal(size=(k + 1, vocab))
+    p = [np.exp(x / temp) / np.exp(x / temp).sum() for x in np.asarray(t_rows, np.float32)]
+    q = [np.exp(x / temp) / np.exp(x / temp).sum() for x in np.asarray(d_rows, np.float32)]
+    d1 = rng.choice(vocab, size=lanes, p=q[0])
+    d2 = rng.choice(vocab, size=lanes, p=q[1])
+    tok = np.full((lanes, k + 1), -1)
+    tok[:, 0], tok[:, 1] = d1, d2
+    f = lambda a, dt: torch.tensor(a, dtype=dt, device=DEV)
+    r = workloads.RoundInputs("mc", vocab, lanes, lanes * (k + 1), "f32",
+                              f(np.tile(t_rows, (lanes, 1)), torch.float32),
+                              f(np.tile(d_rows, (lanes, 1)), torch.float32),
+                              f(tok.reshape(-1), torch.int32), f(np.full(lanes, k), torch.int32),
+                              f(np.arange(lanes + 1) * (k + 1), torch.int32),
+                              f(np.full(lanes, temp), torch.float32), 99)
+    g = run_gpu(r, stats=False)
+    out = g["out_tokens"].reshape(lanes, k + 1)
+    assert (g["lane_status"] == 0).all()
+    t1 = np.bincount(out[:, 0], minlength=vocab)
+    assert stats.chisquare(t1, p[0] * lanes).pvalue > 1e-4
+    acc = g["committed"] >= 2
+    t2 = np.bincount(out[acc, 1], minlength=vocab)
+    assert stats.chisquare(t2, p[1] * acc.sum()).pvalue > 1e-4
+    acc2 = g["committed"] >= 3
+    t3 = np.bincount(out[acc2, 2], minlength=vocab)
+    assert stats.chisquare(t3, p[2] * acc2.sum()).pvalue > 1e-4
+
+
+def _tiny_round(vocab=64, k=3, lanes=4, temp=0.0, seed=3):
+    return workloads.make_custom_round(seed, DEV, lanes=lanes, vocab=vocab, kmax=k, dtype="bf16",
+                                       sampled="none" if temp <= 0 else "all", fixed_k=True)
+
+
+def test_nonfinite_rows_fail_only_their_lane():
+    r = _tiny_round(lanes=5, temp=1.0)
+    off = r.row_offsets.cpu().numpy()
+    r.target[off[1] + 2, 7] = float("nan")
+    r.target[off[2] + 0, 3] = float("inf")
+    r.target[off[3] + 1, :] = float("-inf")
+    r.draft[off[4] + 0, 5] = float("nan")          # a drafter row that is read
+    r.draft[off[0] + 3, 5] = float("nan")          # the lane's last drafter row: never read
+    gpu, orc = run_gpu(r), run_oracle(r)
+    assert gpu["lane_status"].tolist() == [0, 4, 4, 4, 4]
+    compare(r, gpu, orc)
+
+
+def test_negative_infinity_logits_are_allowed():
+    r = _tiny_round(lanes=4, temp=0.0)
+    r.target[:, ::3] = float("-inf")
+    compare(r, run_gpu(r), run_oracle(r))
+    r = _tiny_round(lanes=4, temp=1.0)
+    r.target[:, ::3] = float("-inf")
+    r.draft[:, 1::4] = float("-inf")
+    compare(r, run_gpu(r), run_oracle(r))
+
+
+def test_token_range_layout_and_unsupported_statuses():
+    r = _tiny_round(lanes=4, temp=0.0)
+    off = r.row_offsets.cpu().numpy()
+    r.draft_tokens[off[1] + 1] = 64          # == V
+    r.draft_tokens[off[2]] = -3
+    gpu, orc = run_gpu(r), run_oracle(r)
+    assert gpu["lane_status"].tolist() == [0, 5, 5, 0]
+    compare(r, gpu, orc)
+    # draft_lens disagree with the offsets: layout error, nothing written
+    r = _tiny_round(lanes=4, temp=0.0)
+    r.draft_lens[3] = 2
+    gpu = run_gpu(r)
+    assert gpu["lane_status"].tolist() == [0, 0, 0, 6]
+    assert gpu["committed"][3] == 0
+    # more drafts than the kernel supports
+    r = workloads.make_custom_round(4, DEV, lanes=2, vocab=100, kmax=16, fixed_k=True, sampled="none")
+    gpu = run_gpu(r)
+    assert gpu["lane_status"].tolist() == [2, 2]
+    assert (gpu["out_tokens"] == -1).all()
+
+
+def test_sampled_lane_without_draft_logits_is_an_argument_error():
+    r = _tiny_round(lanes=3, temp=1.0)
+    r.temperatures[0] = 0.0
+    r.draft = None
+    gpu = run_gpu(r)
+    assert gpu["lane_status"].tolist() == [0, 1, 1]
+
+
+def test_host_argument_errors():
+    r = _tiny_round()
+    c = torch.zeros(4, dtype=torch.int32, device=DEV)
+    o = torch.zeros(r.rows, dtype=torch.int32, device=DEV)
+    with pytest.raises(sv.SpecError) as e:
+        sv.spec_verify_accept(r.target, None, r.draft_tokens, r.draft_lens, r.row_offsets,
+                              r.temperatures, 1, c, o, rows=2)  # rows < lanes
+    assert e.value.code == sv.SPEC_ERR_INVALID_ARG
+
+
+def test_identical_draft_and_target_accepts_everything():
+    """q == p: every ratio is 1 > u, so every sampled lane commits k + 1."""
+    r = _tiny_round(vocab=5000, k=6, lanes=8, temp=0.8)
+    r.draft = r.target.clone()
+    gpu, orc = run_gpu(r), run_oracle(r)
+    assert (gpu["committed"] == 7).all()
+    compare(r, gpu, orc)
+
+
+def test_results_do_not_depend_on_the_cluster_shape(monkeypatch):
+    r = workloads.make_custom_round(31, DEV, lanes=6, vocab=70000, kmax=7, dtype="bf16", sampled="mixed")
+    ref = run_gpu(r)
+    orc = run_oracle(r)
+    for c in ("1", "2", "4", "8", "16"):
+        monkeypatch.setenv("SPEC_VERIFY_CLUSTER", c)
+        for slot_kb in ("32", "4"):
+            monkeypatch.setenv("SPEC_VERIFY_SLOT_KB", slot_kb)
+            g = run_gpu(r)
+            compare(r, g, orc)
+            # greedy lanes are bit-identical across shapes
+            greedy = (r.temperatures.cpu().numpy() <= 0)
+            assert (g["committed"][greedy] == ref["committed"][greedy]).all()

@@ -151,8 +151,12 @@ def _per_row(values, lens, offsets):
     return torch.repeat_interleave(values, counts)
 
 
-def make_round(name, seed=0, device="cpu"):
-    """Inputs of one named workload (see the module docstring)."""
+def make_round(name, seed=0, device="cpu", with_state=True):
+    """Inputs of one named workload (see the module docstring).
+
+    ``with_state=False`` skips the recurrent-state snapshots of the commit
+    workload (callers that share one state between several logits sets).
+    """
     device = torch.device(device)
     g = _gen(seed, device)
     philox_seed = (int(seed) * 0x9E3779B97F4A7C15 + 0x5EED) & ((1 << 64) - 1)
@@ -172,7 +176,8 @@ def make_round(name, seed=0, device="cpu"):
         r = _fixed_k_round(name, g, device, lanes=64, k=3, vocab=151936, sigma=2.0,
                            spike=8.0, alpha=0.8, dtype="bf16", temperature=0.0,
                            seed=philox_seed)
-        r.staged, r.live = make_state(64, 4, STATE_SHAPE, seed, device)
+        if with_state:
+            r.staged, r.live = make_state(64, 4, STATE_SHAPE, seed, device)
         return r
     if name == RAGGED_MIXED_B128:
         return _ragged_round(name, g, device, lanes=128, kmax=RAGGED_DRAFT_TOKENS,
