@@ -80,7 +80,9 @@ def test_misaligned_base_takes_elementwise_path():
 def test_many_seeds_mixed(seed):
     r = workloads.make_custom_round(100 + seed, DEV, lanes=64, vocab=12000, kmax=7, dtype="bf16",
                                     sampled="mixed")
-    compare(r, run_gpu(r), run_oracle(r))
+    counts = compare(r, run_gpu(r), run_oracle(r))
+    print(counts)
+    assert counts["accept_flips"] + counts["draw_flips"] <= 2, counts
 
 
 @pytest.mark.parametrize("name", workloads.WORKLOADS)
@@ -93,7 +95,8 @@ def test_named_workloads_full_size(name):
         assert r.rows <= workloads.RAGGED_ROW_BUDGET
     gpu = run_gpu(r)
     orc = run_oracle(r)
-    compare(r, gpu, orc)
+    counts = compare(r, gpu, orc)
+    print(name, counts)
     assert (gpu["committed"] >= 1).all()
     assert (gpu["committed"] <= r.draft_lens.cpu().numpy() + 1).all()
 
@@ -150,8 +153,10 @@ def test_sampled_marginals_on_the_gpu():
     vocab, k, temp, lanes = 6, 2, 0.9, 40000
     t_rows = rng.normal(size=(k + 1, vocab)) * 1.2
     d_rows = t_rows + rng.normal(size=(k + 1, vocab))
-    p = [np.exp(x / temp) / np.exp(x / temp).sum() for x in np.asarray(t_rows, np.float32)]
-    q = [np.exp(x / temp) / np.exp(x / temp).sum() for x in np.asarray(d_rows, np.float32)]
+    t_rows = np.asarray(t_rows, np.float32).astype(np.float64)
+    d_rows = np.asarray(d_rows, np.float32).astype(np.float64)
+    p = [np.exp(x / temp) / np.exp(x / temp).sum() for x in t_rows]
+    q = [np.exp(x / temp) / np.exp(x / temp).sum() for x in d_rows]
     d1 = rng.choice(vocab, size=lanes, p=q[0])
     d2 = rng.choice(vocab, size=lanes, p=q[1])
     tok = np.full((lanes, k + 1), -1)
