@@ -159,6 +159,17 @@ __device__ __forceinline__ void st_cluster_v2(uint32_t addr, uint32_t a, uint32_
   asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
+// Asynchronous stores into a peer CTA's shared memory that count their bytes
+// against an mbarrier in that CTA (both addresses from cluster_map).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+      : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch
 // ---------------------------------------------------------------------------
@@ -177,6 +188,20 @@ __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
+}
+
+// max of two floats; NaN if either is NaN.
+__device__ __forceinline__ float f32_max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// Warp-wide max of a float (all 32 lanes), one instruction on sm_100-family GPUs.
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -201,6 +226,20 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+
+}  // namespace specv
+
+namespace specv {
+
+// log2(x) for finite x > 0 as exponent + log2(mantissa in [1, 2)): the fp32
+// log2 of the mantissa is accurate to about 1e-7 absolute, so the result keeps
+// that absolute accuracy however large the exponent.  log2(0) = -inf.
+__device__ __forceinline__ double log2_split(float x) {
+  if (x == 0.f) return -INFINITY;
+  int e;
+  const float m = frexpf(x, &e);  // x = m * 2^e, m in [0.5, 1)
+  return static_cast<double>(e - 1) + static_cast<double>(log2f(2.f * m));
 }
 
 }  // namespace specv

@@ -90,11 +90,14 @@ VerifyShape choose_shape(int lanes, int V, int esize, bool aligned, int sms, int
   const int64_t slot_max = static_cast<int64_t>(env_int("SPEC_VERIFY_SLOT_KB", 32)) * 1024;
   const int64_t chunks = (slice_bytes + slot_max - 1) / slot_max;
   s.slot_bytes = static_cast<int>(round_up((slice_bytes + chunks - 1) / chunks, 16));
-  const bool many = static_cast<int64_t>(lanes) * C > sms;
-  const int64_t ring = static_cast<int64_t>(env_int("SPEC_VERIFY_RING_KB", many ? 96 : 160)) * 1024;
+  // 88 KB keeps two CTAs per SM possible, so that enough 16-CTA clusters can
+  // be resident at once.
+  const int64_t ring = static_cast<int64_t>(env_int("SPEC_VERIFY_RING_KB", 88)) * 1024;
+  // A multiple of the kernel's consumer-warp groups (each group owns its slots).
   int nslots = static_cast<int>(ring / s.slot_bytes);
-  if (nslots < 2) nslots = 2;
-  if (nslots > specv::kMaxSlots) nslots = specv::kMaxSlots;
+  nslots -= nslots % specv::kGroups;
+  if (nslots < specv::kGroups) nslots = specv::kGroups;
+  if (nslots > specv::kMaxSlots) nslots = specv::kMaxSlots - specv::kMaxSlots % specv::kGroups;
   s.nslots = nslots;
   s.smem = s.head_bytes + nslots * s.slot_bytes;
   return s;

@@ -35,12 +35,23 @@ constexpr int kMaxDrafts = SPEC_MAX_DRAFTS;      // 15
 constexpr int kMaxStreams = 2 * kMaxDrafts + 1;  // target rows + drafter rows of one lane
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kProducerWarp = kConsumerWarps;    // streams the slices (lane 0)
+constexpr int kHelperWarp = kConsumerWarps + 1;  // draft tokens, logits at them, uniforms
+constexpr int kThreads = kConsumers + 64;
 constexpr int kMaxCluster = 16;
 constexpr int kMaxSlots = 16;
 constexpr int kDrawRound = 256;  // elements per warp per pass-2 round (32 lanes x 8)
+constexpr int kPieces = 4;       // warps sharing one chunk of the ring
+// Consumer warps form kGroups groups of kPieces; group g takes the chunks
+// ch = g (mod kGroups).  The ring must have a multiple of kGroups slots so
+// that every slot belongs to one group: a warp then only ever waits on a slot
+// whose previous phase it consumed itself, which keeps the phase parity of
+// mbarrier.try_wait unambiguous.
+constexpr int kGroups = kConsumerWarps / kPieces;
+static_assert(kConsumerWarps % kPieces == 0, "consumer warps must form whole groups");
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr double kLog2eD = 1.4426950408889634;
 constexpr double kLn2d = 0.6931471805599453;
 
 // Partial reduction of one row over some elements (16 bytes, pushed over DSMEM).
@@ -65,6 +76,8 @@ enum DrawMode : int { kNoDraw = 0, kResidual = 1, kBonus = 2 };
 struct __align__(16) SmemHead {
   uint64_t full[kMaxSlots];
   uint64_t empty[kMaxSlots];
+  uint64_t xbar;     // completes when every peer's row partials have landed
+  uint64_t dbar[2];  // the same for the pass-2 slice sums
   Partial wpart[kMaxStreams][kConsumerWarps];  // per consumer warp
   Partial cpart[kMaxCluster][kMaxStreams];     // per CTA of the cluster (pushed by peers)
   Partial fin[kMaxStreams];                    // this CTA's partial, then the lane's total
@@ -74,9 +87,10 @@ struct __align__(16) SmemHead {
   int drafts[kMaxDrafts + 1];
   float xd_t[kMaxDrafts + 1];  // target logit at d_{j+1} in row j
   float xd_q[kMaxDrafts + 1];  // drafter logit at d_{j+1} in row j
+  float u_acc[kMaxDrafts + 1];  // acceptance uniform of position j
+  float u_smp[kMaxDrafts + 1];  // draw uniform of position j
   int scan_n;
   int scan_mode;
-  float scan_u;
   uint32_t cta_flags;
 };
 
@@ -242,24 +256,130 @@ __device__ __forceinline__ void acc_vec(Acc& a, const uint4 v, int e0, float c) 
   }
 }
 
+// Element e of a 16-byte vector as fp32.
+template <typename T>
+__device__ __forceinline__ float vec_elem(const uint4 v, int e) {
+  if constexpr (ElemTraits<T>::kVec == 8) {
+    const uint32_t w = (e < 2) ? v.x : (e < 4) ? v.y : (e < 6) ? v.z : v.w;
+    return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+  } else {
+    const uint32_t w = (e == 0) ? v.x : (e == 1) ? v.y : (e == 2) ? v.z : v.w;
+    return __uint_as_float(w);
+  }
+}
+
+// Largest element of one vector, NaN if any element is NaN.
+template <typename T>
+__device__ __forceinline__ float vec_max_nan(const uint4 v) {
+  if constexpr (ElemTraits<T>::kVec == 8) {
+    const uint32_t h = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
+    return f32_max_nan(bf16_lo(h), bf16_hi(h));
+  } else {
+    return f32_max_nan(f32_max_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                       f32_max_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+}
+
+// Sum of 2^((x - mm) * c) over the elements of one vector.
+template <typename T>
+__device__ __forceinline__ float vec_exp_sum(const uint4 v, float mm, float c) {
+  if constexpr (ElemTraits<T>::kVec == 8) {
+    const float e01 = exp_term(bf16_lo(v.x), mm, c) + exp_term(bf16_hi(v.x), mm, c);
+    const float e23 = exp_term(bf16_lo(v.y), mm, c) + exp_term(bf16_hi(v.y), mm, c);
+    const float e45 = exp_term(bf16_lo(v.z), mm, c) + exp_term(bf16_hi(v.z), mm, c);
+    const float e67 = exp_term(bf16_lo(v.w), mm, c) + exp_term(bf16_hi(v.w), mm, c);
+    return (e01 + e23) + (e45 + e67);
+  } else {
+    return (exp_term(__uint_as_float(v.x), mm, c) + exp_term(__uint_as_float(v.y), mm, c)) +
+           (exp_term(__uint_as_float(v.z), mm, c) + exp_term(__uint_as_float(v.w), mm, c));
+  }
+}
+
+// One piece of a chunk in shared memory, processed by one warp: this lane's
+// vectors are vb + lane, vb + lane + 32, ... below ve.  Phase 1 keeps the
+// largest vector maximum and the first vector holding it, with two independent
+// accumulators so that consecutive vectors do not wait on each other; the
+// lowest element index is then looked up in that one vector, and only if it
+// beats the running max.  Phase 2 (sampled rows) sums the exponentials at the
+// now fixed max with four independent partial sums.
+template <typename T, bool SAMPLED>
+__device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int ve, int ebase, float c,
+                                          int lane) {
+  constexpr int kVec = ElemTraits<T>::kVec;
+  float m0 = -INFINITY, m1 = -INFINITY, nanacc = -INFINITY;
+  int i0 = INT_MAX, i1 = INT_MAX;
+  int v = vb + lane;
+  for (; v + 32 < ve; v += 64) {
+    const float a0 = vec_max_nan<T>(sv[v]);
+    const float a1 = vec_max_nan<T>(sv[v + 32]);
+    nanacc = f32_max_nan(nanacc, f32_max_nan(a0, a1));
+    if (a0 > m0) {
+      m0 = a0;
+      i0 = v;
+    }
+    if (a1 > m1) {
+      m1 = a1;
+      i1 = v + 32;
+    }
+  }
+  if (v < ve) {
+    const float a0 = vec_max_nan<T>(sv[v]);
+    nanacc = f32_max_nan(nanacc, a0);
+    if (a0 > m0) {
+      m0 = a0;
+      i0 = v;
+    }
+  }
+  if (nanacc != nanacc || nanacc == INFINITY) a.bad = 1;
+  if (m1 > m0 || (m1 == m0 && i1 < i0)) {
+    m0 = m1;
+    i0 = i1;
+  }
+  if (m0 > a.m) {
+    const uint4 x = sv[i0];
+    int e = 0;
+#pragma unroll
+    for (int t = kVec - 1; t >= 0; --t)
+      if (vec_elem<T>(x, t) == m0) e = t;
+    acc_raise<SAMPLED>(a, m0, ebase + i0 * kVec + e, c);
+  }
+  if (SAMPLED) {
+    const float mm = (a.m == -INFINITY) ? 0.f : a.m;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    int w = vb + lane;
+    for (; w + 96 < ve; w += 128) {
+      s0 += vec_exp_sum<T>(sv[w], mm, c);
+      s1 += vec_exp_sum<T>(sv[w + 32], mm, c);
+      s2 += vec_exp_sum<T>(sv[w + 64], mm, c);
+      s3 += vec_exp_sum<T>(sv[w + 96], mm, c);
+    }
+    for (; w < ve; w += 32) s0 += vec_exp_sum<T>(sv[w], mm, c);
+    a.s += (s0 + s1) + (s2 + s3);
+  }
+}
+
 __device__ __forceinline__ uint32_t acc_bad(const Acc& a) {
   const float lo = bf16_lo(a.nan2), hi = bf16_hi(a.nan2);
   const bool packed_bad = (lo != lo) || (hi != hi) || lo == INFINITY || hi == INFINITY;
   return (a.bad || packed_bad) ? kBadValue : 0u;
 }
 
-// Warp-wide merge; every lane ends with the warp's partial.
+// Warp-wide merge; every lane ends with the warp's max, lowest index of the
+// max and flags, lane 0 with the sum.  The max and the index are single warp
+// reductions; each lane then rescales its own sum to the warp max once and
+// the sums are added by a butterfly.
 template <bool SAMPLED>
 __device__ __forceinline__ Partial warp_merge(float m, float s, int idx, uint32_t flags, float c) {
+  flags = __reduce_or_sync(0xFFFFFFFFu, flags);
+  const float M = warp_max_f32(m);
+  const int I = __reduce_min_sync(0xFFFFFFFFu, (m == M) ? idx : INT_MAX);
+  if (SAMPLED) {
+    float t = (M == -INFINITY) ? s : s * ex2_approx((m - M) * c);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-    const int i2 = __shfl_xor_sync(0xFFFFFFFFu, idx, o);
-    flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, o);
-    merge_part<SAMPLED>(m, s, idx, m2, s2, i2, c);
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+    s = t;
   }
-  return Partial{m, s, idx, flags};
+  return Partial{M, s, I, flags};
 }
 
 __device__ __forceinline__ Partial identity_partial() { return Partial{-INFINITY, 0.f, INT_MAX, 0u}; }
@@ -347,8 +467,29 @@ __device__ __forceinline__ int warp_max_int(int v) {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
+
+// Push this CTA's partial of every row into the CTAs that need it: the leader
+// only for greedy lanes, every CTA of the cluster for sampled lanes.  A peer's
+// copy goes by st.async and completes the receiver's xbar; the CTA's own copy
+// is a plain shared-memory store.
+__device__ __forceinline__ void push_partials(SmemHead& sh, int nstreams, int C, uint32_t rank,
+                                              bool to_all, uint32_t extra_flags) {
+  const int dests = to_all ? C : 1;
+  for (int t = threadIdx.x; t < nstreams * dests; t += kThreads) {
+    const int s = t / dests, dst = t % dests;
+    const Partial q = sh.fin[s];
+    const uint32_t fl = q.flags | extra_flags;
+    if (dst == static_cast<int>(rank)) {
+      sh.cpart[rank][s] = Partial{q.m, q.s, q.idx, fl};
+    } else {
+      st_async_v4(cluster_map(&sh.cpart[rank][s], dst), __float_as_uint(q.m), __float_as_uint(q.s),
+                  static_cast<uint32_t>(q.idx), fl, cluster_map(&sh.xbar, dst));
+    }
+  }
+}
+
 template <typename T, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads, 2) verify_accept_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(kThreads, 1) verify_accept_kernel(const VerifyParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SmemHead& sh = *reinterpret_cast<SmemHead*>(smem_raw);
   uint8_t* ring = smem_raw + p.head_bytes;
@@ -361,20 +502,21 @@ __global__ void __launch_bounds__(kThreads, 2) verify_accept_kernel(const Verify
   const int lane = tid & 31;
   const int C = p.cluster;
   const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
   const int b = blockIdx.x / C;
 
   // ---- set-up that touches only shared memory (overlaps the previous kernel) ----
   if (tid == 0) {
-    for (int s = 0; s < p.nslots; ++s) {
+    for (int s = 0; s < p.nslots - p.nslots % kGroups; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], kConsumerWarps);
+      mbar_init(&sh.empty[s], kPieces);
     }
+    mbar_init(&sh.xbar, 1);
+    mbar_init(&sh.dbar[0], 1);
+    mbar_init(&sh.dbar[1], 1);
     sh.cta_flags = 0;
     fence_mbar_init();
   }
-  // Phase A of the cluster barrier: every CTA of the cluster has started.  It is
-  // waited on just before the first write into a peer's shared memory.
-  cluster_arrive_relaxed();
   griddep_wait();
 
   // ---- lane metadata (read by every thread; one transaction per warp) ----
@@ -399,8 +541,24 @@ __global__ void __launch_bounds__(kThreads, 2) verify_accept_kernel(const Verify
   const int span = v1 - v0;
   const int body = ALIGNED ? (span / kVec) * kVec : 0;
   const int slot_elems = p.slot_bytes / kEsize;
+  const int nslots = p.nslots - p.nslots % kGroups;  // a multiple of kGroups (host ensures >= kGroups)
 
+  // Bytes this CTA will receive from its peers: their partial of every row
+  // (leader of a greedy lane, or every CTA of a sampled lane), then for
+  // sampled lanes their pass-2 slice sums.  Announced before this CTA arrives
+  // on the cluster barrier, so before any peer can push.
+  if (tid == 0) {
+    const bool receives = sampled || leader;
+    mbar_arrive_expect_tx(&sh.xbar, receives ? static_cast<uint32_t>((C - 1) * nstreams * 16) : 0u);
+    if (sampled) {
+      mbar_arrive_expect_tx(&sh.dbar[0], static_cast<uint32_t>((C - 1) * 16));
+      mbar_arrive_expect_tx(&sh.dbar[1], static_cast<uint32_t>((C - 1) * 16));
+    }
+  }
   __syncthreads();  // barrier initialisation visible to every thread
+  // Every CTA of the cluster has started once this phase completes; it is
+  // waited on just before the first store into a peer's shared memory.
+  cluster_arrive_relaxed();
 
   // Row of stream s: sampled lanes interleave target row j (even s) and drafter
   // row j (odd s); greedy lanes read target rows only.
@@ -411,94 +569,130 @@ __global__ void __launch_bounds__(kThreads, 2) verify_accept_kernel(const Verify
   };
 
   // ---- pass 1 ----
-  if (warp == kConsumerWarps) {
-    // Producer warp.  Lane 0 streams the slices; lanes 1.. fetch the draft tokens
-    // and, for sampled lanes, the logits at the draft tokens.
-    if (lane == 0) {
-      if (ALIGNED) {
-        uint32_t it = 0;
-        bool ok = true;
-        for (int s = 0; s < nstreams && ok; ++s) {
-          const uint8_t* row = stream_row(s) + static_cast<int64_t>(v0) * kEsize;
-          for (int c0 = 0; c0 < body; c0 += slot_elems) {
-            const int L = min(slot_elems, body - c0);
-            const uint32_t slot = it % p.nslots;
-            const uint32_t par = (it / p.nslots) & 1u;
-            if (!mbar_wait_bounded(&sh.empty[slot], par ^ 1u)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&sh.full[slot], static_cast<uint32_t>(L * kEsize));
-            bulk_g2s(ring + static_cast<size_t>(slot) * p.slot_bytes, row + static_cast<int64_t>(c0) * kEsize,
-                     static_cast<uint32_t>(L * kEsize), &sh.full[slot]);
-            ++it;
-          }
-        }
-        // Drain: every copy issued has landed before shared memory is reused.
-        const uint32_t first = it > static_cast<uint32_t>(p.nslots) ? it - p.nslots : 0u;
-        for (uint32_t i = first; i < it; ++i)
-          if (!mbar_wait_bounded(&sh.full[i % p.nslots], (i / p.nslots) & 1u)) ok = false;
-        if (!ok) atomicOr(&sh.cta_flags, kTimedOut);
-      }
-    } else if (lane - 1 < k && status == SPEC_OK) {
-      const int j = lane - 1;
-      const int d = __ldg(p.draft_tokens + off + j);
-      sh.drafts[j] = d;
-      if (sampled && d >= 0 && d < p.V) {
-        sh.xd_t[j] = ElemTraits<T>::load(p.target + static_cast<int64_t>(off + j) * p.ld_bytes, d);
-        sh.xd_q[j] = ElemTraits<T>::load(p.draft + static_cast<int64_t>(off + j) * p.ld_bytes, d);
-      }
-    }
-  } else {
-    // Consumer warps.
-    uint32_t it = 0;
-    bool ok = true;
-    for (int s = 0; s < nstreams; ++s) {
-      Acc a;
-      acc_init(a);
-      const uint8_t* row = stream_row(s);
-      if (ALIGNED) {
-        for (int c0 = 0; c0 < body && ok; c0 += slot_elems) {
+  if (warp == kProducerWarp) {
+    if (lane == 0 && ALIGNED) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int s = 0; s < nstreams && ok; ++s) {
+        const uint8_t* row = stream_row(s) + static_cast<int64_t>(v0) * kEsize;
+        for (int c0 = 0; c0 < body; c0 += slot_elems) {
           const int L = min(slot_elems, body - c0);
-          const uint32_t slot = it % p.nslots;
-          const uint32_t par = (it / p.nslots) & 1u;
-          if (!mbar_wait_bounded(&sh.full[slot], par)) {
+          const uint32_t slot = it % nslots;
+          const uint32_t par = (it / nslots) & 1u;
+          if (!mbar_wait_bounded(&sh.empty[slot], par ^ 1u)) {
             ok = false;
             break;
           }
-          const uint4* sv = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * p.slot_bytes);
-          const int nvec = L / kVec;
-          const int ebase = v0 + c0;
-          if (sampled) {
-#pragma unroll 4
-            for (int v = tid; v < nvec; v += kConsumers) acc_vec<T, true>(a, sv[v], ebase + v * kVec, c);
-          } else {
-#pragma unroll 4
-            for (int v = tid; v < nvec; v += kConsumers) acc_vec<T, false>(a, sv[v], ebase + v * kVec, c);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.empty[slot]);
+          mbar_arrive_expect_tx(&sh.full[slot], static_cast<uint32_t>(L * kEsize));
+          bulk_g2s(ring + static_cast<size_t>(slot) * p.slot_bytes, row + static_cast<int64_t>(c0) * kEsize,
+                   static_cast<uint32_t>(L * kEsize), &sh.full[slot]);
           ++it;
         }
       }
-      // Elements outside the bulk-copied body: the row tail, or the whole slice
-      // when rows are not 16-byte aligned.
-      for (int e = body + tid; e < span && ok; e += kConsumers) {
-        const float x = ElemTraits<T>::load(row, v0 + e);
-        if (sampled) acc_scalar<true>(a, x, v0 + e, c);
-        else acc_scalar<false>(a, x, v0 + e, c);
+      // Drain: every copy issued has landed before shared memory is reused.
+      const uint32_t first = it > static_cast<uint32_t>(nslots) ? it - nslots : 0u;
+      for (uint32_t i = first; i < it; ++i)
+        if (!mbar_wait_bounded(&sh.full[i % nslots], (i / nslots) & 1u)) ok = false;
+      if (!ok) atomicOr(&sh.cta_flags, kTimedOut);
+    }
+  } else if (warp == kHelperWarp) {
+    // Draft tokens, the logits at them and the lane's uniforms, while the
+    // slices stream in.  Lane j handles position j.
+    if (status == SPEC_OK && lane <= k) {
+      const int j = lane;
+      if (j < k) {
+        const int d = __ldg(p.draft_tokens + off + j);
+        sh.drafts[j] = d;
+        if (sampled && d >= 0 && d < p.V) {
+          sh.xd_t[j] = ElemTraits<T>::load(p.target + static_cast<int64_t>(off + j) * p.ld_bytes, d);
+          sh.xd_q[j] = ElemTraits<T>::load(p.draft + static_cast<int64_t>(off + j) * p.ld_bytes, d);
+        }
       }
-      const uint32_t fl = acc_bad(a) | (ok ? 0u : kTimedOut);
-      const Partial wp = sampled ? warp_merge<true>(a.m, a.s, a.idx, fl, c)
-                                 : warp_merge<false>(a.m, a.s, a.idx, fl, c);
-      if (lane == 0) sh.wpart[s][warp] = wp;
+      if (sampled) {
+        const float2 u = round_uniforms(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(j));
+        sh.u_acc[j] = u.x;
+        sh.u_smp[j] = u.y;
+      }
+    }
+  } else {
+    // Consumer warps.  The work items are (chunk, piece): chunk ch of the ring
+    // sequence is split into kPieces ranges of vectors, and warp w takes items
+    // w, w + 8, ...  Warps therefore work on different chunks at once and only
+    // meet at the end.  A warp merges its lanes only when its row changes.
+    for (int s = 0; s < nstreams; ++s)
+      if (lane == 0) sh.wpart[s][warp] = identity_partial();
+    bool ok = true;
+    if (ALIGNED && body > 0) {
+      const int nch = (body + slot_elems - 1) / slot_elems;  // chunks per row
+      const int items = nstreams * nch * kPieces;
+      int cur = -1;
+      Acc a;
+      acc_init(a);
+      for (int i = warp; i < items && ok; i += kConsumerWarps) {
+        const int ch = i / kPieces, q = i % kPieces;
+        const int s = ch / nch, ci = ch % nch;
+        if (s != cur) {
+          if (cur >= 0) {
+            const Partial wp = sampled ? warp_merge<true>(a.m, a.s, a.idx, acc_bad(a), c)
+                                       : warp_merge<false>(a.m, a.s, a.idx, acc_bad(a), c);
+            if (lane == 0) sh.wpart[cur][warp] = wp;
+          }
+          acc_init(a);
+          cur = s;
+        }
+        const uint32_t slot = static_cast<uint32_t>(ch) % nslots;
+        const uint32_t par = (static_cast<uint32_t>(ch) / nslots) & 1u;
+        if (!mbar_wait_bounded(&sh.full[slot], par)) {
+          ok = false;
+          break;
+        }
+        const uint4* sv = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * p.slot_bytes);
+        const int c0 = ci * slot_elems;
+        const int nvec = min(slot_elems, body - c0) / kVec;
+        const int per = (nvec + kPieces - 1) / kPieces;
+        const int vb = min(nvec, q * per), ve = min(nvec, vb + per);
+        if (sampled) acc_range<T, true>(a, sv, vb, ve, v0 + c0, c, lane);
+        else acc_range<T, false>(a, sv, vb, ve, v0 + c0, c, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.empty[slot]);
+      }
+      if (cur >= 0) {
+        const uint32_t fl = acc_bad(a) | (ok ? 0u : kTimedOut);
+        const Partial wp = sampled ? warp_merge<true>(a.m, a.s, a.idx, fl, c)
+                                   : warp_merge<false>(a.m, a.s, a.idx, fl, c);
+        if (lane == 0) sh.wpart[cur][warp] = wp;
+      }
+    }
+    // Elements outside the bulk-copied body: the row tail, or the whole slice
+    // when rows are not 16-byte aligned.  Each warp folds them into its own
+    // entry of every row.
+    if (span > body && ok) {
+      for (int s = 0; s < nstreams; ++s) {
+        const uint8_t* row = stream_row(s);
+        Acc a;
+        acc_init(a);
+        for (int e = body + tid; e < span; e += kConsumers) {
+          const float x = ElemTraits<T>::load(row, v0 + e);
+          if (sampled) acc_scalar<true>(a, x, v0 + e, c);
+          else acc_scalar<false>(a, x, v0 + e, c);
+        }
+        const Partial wp = sampled ? warp_merge<true>(a.m, a.s, a.idx, acc_bad(a), c)
+                                   : warp_merge<false>(a.m, a.s, a.idx, acc_bad(a), c);
+        if (lane == 0) {
+          Partial o = sh.wpart[s][warp];
+          if (sampled) merge_part<true>(o.m, o.s, o.idx, wp.m, wp.s, wp.idx, c);
+          else merge_part<false>(o.m, o.s, o.idx, wp.m, wp.s, wp.idx, c);
+          o.flags |= wp.flags;
+          sh.wpart[s][warp] = o;
+        }
+      }
     }
     if (!ok && lane == 0) atomicOr(&sh.cta_flags, kTimedOut);
   }
   __syncthreads();
   griddep_launch_dependents();
 
-  // ---- CTA partial of every row -> pushed to every CTA of the cluster ----
+  // ---- this CTA's partial of every row ----
   if (warp < kConsumerWarps) {
     for (int s = warp; s < nstreams; s += kConsumerWarps) {
       const Partial q = (lane < kConsumerWarps) ? sh.wpart[s][lane] : identity_partial();
@@ -508,23 +702,13 @@ __global__ void __launch_bounds__(kThreads, 2) verify_accept_kernel(const Verify
     }
   }
   __syncthreads();
-  cluster_wait_acquire();  // phase A: all peers are running
-  {
-    const uint32_t extra = sh.cta_flags;
-    for (int t = tid; t < nstreams * C; t += kThreads) {
-      const int s = t / C, dst = t % C;
-      const Partial q = sh.fin[s];
-      st_cluster_v4(cluster_map(&sh.cpart[rank][s], dst), __float_as_uint(q.m), __float_as_uint(q.s),
-                    static_cast<uint32_t>(q.idx), q.flags | extra);
-    }
-  }
-  cluster_arrive_release();
-  cluster_wait_acquire();  // phase B: every partial has arrived
-
-  const bool leader = (rank == 0);
-  if (!sampled && !leader) return;  // greedy lanes: only the leader finishes
+  cluster_wait_acquire();  // every peer is running: its shared memory may be written
+  push_partials(sh, nstreams, C, rank, sampled, sh.cta_flags);
+  if (!sampled && !leader) return;  // greedy lanes: the leader finishes alone
 
   // ---- the lane's totals ----
+  if (tid == 0 && !mbar_wait_bounded(&sh.xbar, 0)) atomicOr(&sh.cta_flags, kTimedOut);
+  __syncthreads();
   if (warp < kConsumerWarps) {
     for (int s = warp; s < nstreams; s += kConsumerWarps) {
       const Partial q = (lane < C) ? sh.cpart[lane][s] : identity_partial();
@@ -561,12 +745,11 @@ __global__ void __launch_bounds__(kThreads, 2) verify_accept_kernel(const Verify
     }
 
     int n = 0, mode = kNoDraw;
-    float uprime = 0.f;
-    // log2 p_j(d), log2 q_j(d) at this lane's position.  The scan touches at most
-    // 15 positions, so it runs in fp64: the only fp32 inputs are the row maxima,
-    // the sums S and the logits themselves.
+    // log2 p_j(d) and log2 q_j(d) at this lane's position:
+    //   (x_d - max) * log2(e) / T - log2(S)
+    // The difference x_d - max is exact, the rest is done in fp64 from an
+    // fp64 1/T and an accurate log2 of S, so they carry ~1e-7 absolute error.
     double lp = NAN, lq = NAN;
-    const double c64 = sampled ? 1.4426950408889634 / static_cast<double>(temp) : 0.0;
     if (st == SPEC_OK) {
       const bool active = lane < k;
       bool stop;
@@ -576,29 +759,23 @@ __global__ void __launch_bounds__(kThreads, 2) verify_accept_kernel(const Verify
       } else {
         bool accept = true;
         if (active) {
+          const double c64 = kLog2eD / static_cast<double>(temp);
           const Partial pt = sh.fin[2 * lane], pq = sh.fin[2 * lane + 1];
-          lp = (static_cast<double>(sh.xd_t[lane]) - pt.m) * c64 - log2(static_cast<double>(pt.s));
-          lq = (static_cast<double>(sh.xd_q[lane]) - pq.m) * c64 - log2(static_cast<double>(pq.s));
-          const float u = round_uniforms(p.seed, b, lane).x;
+          lp = static_cast<double>(sh.xd_t[lane] - pt.m) * c64 - log2_split(pt.s);
+          lq = static_cast<double>(sh.xd_q[lane] - pq.m) * c64 - log2_split(pq.s);
           if (lp == -INFINITY) accept = false;
           else if (lq == -INFINITY) accept = true;
-          else accept = log2(static_cast<double>(u)) < lp - lq;
+          else accept = log2_split(sh.u_acc[lane]) < lp - lq;
         }
         stop = active && !accept;
       }
       const uint32_t mask = __ballot_sync(0xFFFFFFFFu, stop);
       n = mask ? (__ffs(mask) - 1) : k;
-      if (sampled) {
-        mode = (n < k) ? kResidual : kBonus;
-        float u2 = 0.f;
-        if (lane <= k) u2 = round_uniforms(p.seed, b, lane).y;
-        uprime = __shfl_sync(0xFFFFFFFFu, u2, n);
-      }
+      if (sampled) mode = (n < k) ? kResidual : kBonus;
     }
     if (lane == 0) {
       sh.scan_n = n;
       sh.scan_mode = (st == SPEC_OK) ? mode : kNoDraw;
-      sh.scan_u = uprime;
     }
 
     // ---- outputs (leader) ----
@@ -622,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_accept_kernel(const Verify
           rs->argmax = pt.idx;
           rs->max_logit = pt.m;
           if (sampled) {
-            rs->lse = static_cast<float>(static_cast<double>(pt.m) / temp + log(static_cast<double>(pt.s)));
+            rs->lse = static_cast<float>(static_cast<double>(pt.m) / temp + log2_split(pt.s) * kLn2d);
             rs->logp_d = (j < k) ? static_cast<float>(lp * kLn2d) : NAN;
             rs->logq_d = (j < k) ? static_cast<float>(lq * kLn2d) : NAN;
           } else {
@@ -646,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_accept_kernel(const Verify
   bool residual = (sh.scan_mode == kResidual);
   int draw_row = residual ? n : k;  // target row whose p enters the weights
   const uint8_t* qrow = p.draft + static_cast<int64_t>(off + n) * p.ld_bytes;
-  const float uprime = sh.scan_u;
+  const float uprime = sh.u_smp[n];
   const int seg = ((span + kConsumerWarps - 1) / kConsumerWarps + kDrawRound - 1) / kDrawRound * kDrawRound;
   auto make_coef = [&]() {
     DrawCoef kc;
@@ -700,10 +877,15 @@ __global__ void __launch_bounds__(kThreads, 2) verify_accept_kernel(const Verify
         wc = __fadd_rn(wc, sh.segsum[w]);
         lc = max(lc, sh.seglast[w]);
       }
-      st_cluster_v2(cluster_map(&sh.dpart[buf][rank], tid), __float_as_uint(wc), static_cast<uint32_t>(lc));
+      if (tid == static_cast<int>(rank)) {
+        sh.dpart[buf][rank] = DrawPartial{wc, lc, 0, 0};
+      } else {
+        st_async_v4(cluster_map(&sh.dpart[buf][rank], tid), __float_as_uint(wc), static_cast<uint32_t>(lc),
+                    0u, 0u, cluster_map(&sh.dbar[buf], tid));
+      }
     }
-    cluster_arrive_release();
-    cluster_wait_acquire();
+    if (tid == 0 && !mbar_wait_bounded(&sh.dbar[buf], 0)) atomicOr(&sh.cta_flags, kTimedOut);
+    __syncthreads();
 
     W = 0.f;
     for (int r = 0; r < C; ++r) W = __fadd_rn(W, sh.dpart[buf][r].w);

@@ -270,3 +270,44 @@ def test_results_do_not_depend_on_the_cluster_shape(monkeypatch):
             # greedy lanes are bit-identical across shapes
             greedy = (r.temperatures.cpu().numpy() <= 0)
             assert (g["committed"][greedy] == ref["committed"][greedy]).all()
+
+
+@pytest.mark.parametrize("cluster,ring_kb,slot_kb", [("4", "75", "32"), ("12", "75", "32"), ("16", "88", "32"),
+                                                      ("8", "40", "8"), ("2", "100", "32")])
+def test_back_to_back_graph_launches_are_identical(monkeypatch, cluster, ring_kb, slot_kb):
+    """50 launches captured in one CUDA graph (the kernels overlap through
+    programmatic dependent launch), each into its own outputs: every launch
+    must give the same results, equal to the oracle's.  Ring shapes that would
+    leave an odd number of slots are included on purpose."""
+    monkeypatch.setenv("SPEC_VERIFY_CLUSTER", cluster)
+    monkeypatch.setenv("SPEC_VERIFY_RING_KB", ring_kb)
+    monkeypatch.setenv("SPEC_VERIFY_SLOT_KB", slot_kb)
+    r = workloads.make_custom_round(77, DEV, lanes=12, vocab=151936, kmax=5, dtype="bf16",
+                                    sampled="mixed", fixed_k=True)
+    n = 50
+    outs = [(torch.zeros(r.lanes, dtype=torch.int32, device=DEV),
+             torch.zeros(r.rows, dtype=torch.int32, device=DEV),
+             torch.zeros(r.lanes, dtype=torch.int32, device=DEV)) for _ in range(n)]
+    stream = torch.cuda.Stream()
+
+    def launch(o):
+        sv.spec_verify_accept(r.target, r.draft, r.draft_tokens, r.draft_lens, r.row_offsets,
+                              r.temperatures, r.seed, o[0], o[1], o[2], stream=torch.cuda.current_stream())
+
+    with torch.cuda.stream(stream):
+        launch(outs[0])  # sets kernel attributes before capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for o in outs:
+                launch(o)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    orc = run_oracle(r)
+    first = {"committed": outs[0][0].cpu().numpy(), "out_tokens": outs[0][1].cpu().numpy(),
+             "lane_status": outs[0][2].cpu().numpy()}
+    compare(r, first, orc, check_stats=False)
+    for o in outs[1:]:
+        assert torch.equal(o[0], outs[0][0]) and torch.equal(o[1], outs[0][1]) and torch.equal(o[2], outs[0][2])
