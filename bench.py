@@ -192,9 +192,11 @@ class Bench:
                 committed=torch.zeros(s.lanes, dtype=torch.int32, device=device),
                 out_tokens=torch.zeros(s.rows, dtype=torch.int32, device=device),
                 status=torch.zeros(s.lanes, dtype=torch.int32, device=device)))
+        # Ranks verify disjoint lane ranges of one notional batch: lane_base keys
+        # their uniforms by global lane index.
         self.args = [sv.make_args(s.target, s.draft, s.draft_tokens, s.draft_lens, s.row_offsets,
                                   s.temperatures, s.seed, o["committed"], o["out_tokens"], o["status"],
-                                  rows=s.rows)
+                                  rows=s.rows, lane_base=rank * s.lanes)
                      for s, o in zip(self.sets, self.outs)]
         self.verify_bytes, self.rows_per_step = round_bytes(first)
         self.has_state = first.staged is not None
@@ -529,6 +531,27 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_launch_only(args):
+    """Profiler driver: build the workload, run N eager steps, no timing."""
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    import speculative_decoding_verify_bf16_gb300 as sv
+    sv.build_library()
+    sv.load_library()
+    r = workloads.make_round(args.workload, seed=args.seed, device=device, commit_lanes=args.commit_lanes)
+    committed = torch.zeros(r.lanes, dtype=torch.int32, device=device)
+    out = torch.zeros(r.rows, dtype=torch.int32, device=device)
+    status = torch.zeros(r.lanes, dtype=torch.int32, device=device)
+    for i in range(args.launch_only):
+        sv.spec_verify_accept(r.target, r.draft, r.draft_tokens, r.draft_lens, r.row_offsets,
+                              r.temperatures, r.seed, committed, out, status)
+        if r.staged is not None:
+            sv.spec_commit_state(r.staged, r.live, committed, status)
+    torch.cuda.synchronize()
+    assert (status.cpu() == 0).all()
+    print(json.dumps({"launch_only": args.launch_only, "workload": args.workload, "lanes": r.lanes}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -541,7 +564,14 @@ def main():
                     help="measure only --workload (by default the other workloads are measured "
                          "too and reported under 'workloads')")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch-only", type=int, default=0, metavar="N",
+                    help="profiler driver: run N eager steps of --workload and exit (no timing)")
+    ap.add_argument("--commit-lanes", type=int, default=None,
+                    help="with --launch-only: lanes of the commit workload (smaller captures)")
     args = ap.parse_args()
+    if args.launch_only:
+        run_launch_only(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -110,6 +110,10 @@ typedef struct {
                                    for i < c_b, -1 for c_b <= i <= k_b            */
   int32_t* lane_status;         /* out [lanes]: spec_status per lane (may be NULL) */
   spec_row_stats* row_stats;    /* out [rows] (may be NULL)                        */
+  uint32_t lane_base;           /* global index of lane 0 in the Philox counter: a batch
+                                   split into parts (GPUs, streams) with lane_base = the
+                                   part's first global lane draws exactly the uniforms
+                                   of the unsplit batch; 0 otherwise                */
 } spec_verify_args;
 
 /*
@@ -127,7 +131,7 @@ typedef struct {
  * normalised, or from p_{k_b} if every draft was accepted -- the acceptance rule
  * the strata2signal page cites from Leviathan et al. (2022) as the one that keeps
  * the target's distribution.  The uniforms come from Philox4x64-10 (Salmon et
- * al., SC'11) with key (seed, 0) and counter (j, b, 0, 0): word 0 gives u_j,
+ * al., SC'11) with key (seed, 0) and counter (j, lane_base + b, 0, 0): word 0 gives u_j,
  * word 1 gives the draw's u'; u = (word >> 40) * 2^-24.  The draw walks token ids
  * upwards and takes the first whose cumulative weight exceeds u' * W.
  *
@@ -177,11 +181,13 @@ int spec_commit_state(const void* staged, void* live, const int32_t* committed,
  * draft at position j of lane b) and out[... + 1] = u'_j (the uniform of an
  * inverse-CDF draw made at position j), for b < lanes and j < positions, from
  * the same device Philox4x64-10 stream the verify kernel uses (key (seed, 0),
- * counter (j, b, 0, 0), u = (word >> 40) * 2^-24).  `out` is a device float
- * array of lanes * positions * 2 entries.  Returns SPEC_ERR_INVALID_ARG for a
- * NULL `out` or negative sizes, SPEC_ERR_CUDA if the launch fails.
+ * counter (j, lane_base + b, 0, 0), u = (word >> 40) * 2^-24).  `out` is a
+ * device float array of lanes * positions * 2 entries.  Returns
+ * SPEC_ERR_INVALID_ARG for a NULL `out` or negative sizes, SPEC_ERR_CUDA if the
+ * launch fails.
  */
-int spec_round_uniforms(uint64_t seed, int32_t lanes, int32_t positions, float* out, void* stream);
+int spec_round_uniforms(uint64_t seed, uint32_t lane_base, int32_t lanes, int32_t positions, float* out,
+                        void* stream);
 
 /* Human-readable name of a spec_status value (static storage, never NULL). */
 const char* spec_status_string(int status);
@@ -191,11 +197,13 @@ const char* spec_status_string(int status);
  *
  * Host-only.  Reports the CTAs per lane (one thread-block cluster per lane),
  * threads per CTA, the vocabulary slice each CTA reduces, and the dynamic shared
- * memory per CTA, for a verify over `lanes` lanes of vocabulary V in `dtype` on
- * the current device.  Any output pointer may be NULL.  Returns SPEC_OK,
- * SPEC_ERR_INVALID_ARG or SPEC_ERR_CUDA.
+ * memory per CTA, for a verify over `lanes` lanes and `rows` rows of vocabulary
+ * V in `dtype` with 16-byte aligned rows on the current device, before any
+ * reduction of the cluster that the device's scheduling limits may force.
+ * Any output pointer may be NULL.  Returns SPEC_OK, SPEC_ERR_INVALID_ARG or
+ * SPEC_ERR_CUDA.
  */
-int spec_verify_launch_shape(int32_t lanes, int32_t V, spec_dtype dtype, int32_t* cluster_ctas,
+int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype dtype, int32_t* cluster_ctas,
                              int32_t* threads, int32_t* slice, int32_t* smem_bytes);
 
 #ifdef __cplusplus

@@ -228,7 +228,7 @@ def _lane_layout_ok(b, k, off, rows):
 
 
 def verify_round(target, draft, draft_tokens, draft_lens, row_offsets,
-                 temperatures, seed=0, u_acc=None, u_smp=None):
+                 temperatures, seed=0, u_acc=None, u_smp=None, lane_base=0):
     """One verify round over all lanes.
 
     target        float64 [rows, V] target logits (already decoded)
@@ -241,6 +241,8 @@ def verify_round(target, draft, draft_tokens, draft_lens, row_offsets,
     seed          Philox key for the uniforms (see ``philox.round_uniforms``)
     u_acc, u_smp  optional [lanes, >= k_b + 1] arrays of uniforms that replace
                   the Philox ones (used by tests that enumerate the uniforms)
+    lane_base     global index of lane 0 in the Philox counter (a batch split
+                  into parts draws the uniforms of the unsplit batch)
     """
     target = np.asarray(target, dtype=np.float64)
     rows, vocab = target.shape
@@ -294,7 +296,7 @@ def verify_round(target, draft, draft_tokens, draft_lens, row_offsets,
             us = [None] * (k + 1)
             for j in range(k + 1):
                 if u_acc is None or u_smp is None:
-                    ua[j], us[j] = philox.round_uniforms(seed, b, j)
+                    ua[j], us[j] = philox.round_uniforms(seed, lane_base + b, j)
                 if u_acc is not None:
                     ua[j] = float(u_acc[b][j])
                 if u_smp is not None:

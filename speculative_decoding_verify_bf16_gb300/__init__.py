@@ -65,6 +65,7 @@ class _Args(ctypes.Structure):
         ("out_tokens", ctypes.c_void_p),
         ("lane_status", ctypes.c_void_p),
         ("row_stats", ctypes.c_void_p),
+        ("lane_base", ctypes.c_uint32),
     ]
 
 
@@ -92,10 +93,10 @@ def load_library():
     lib.spec_status_string.restype = ctypes.c_char_p
     lib.spec_status_string.argtypes = [ctypes.c_int]
     lib.spec_round_uniforms.restype = ctypes.c_int
-    lib.spec_round_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
+    lib.spec_round_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_void_p, ctypes.c_void_p]
     lib.spec_verify_launch_shape.restype = ctypes.c_int
-    lib.spec_verify_launch_shape.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int] + \
+    lib.spec_verify_launch_shape.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int] + \
         [ctypes.POINTER(ctypes.c_int32)] * 4
     _lib = lib
     return lib
@@ -149,7 +150,7 @@ def row_stats_view(buf):
 
 def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, temperatures, seed,
                        committed, out_tokens, lane_status=None, row_stats=None, stream=None,
-                       rows=None):
+                       rows=None, lane_base=0):
     """Launch the fused verify kernel (see spec_verify_accept in include/spec_verify.h).
 
     target, draft: [rows, >= V] bf16 or float32 CUDA tensors with unit inner
@@ -158,6 +159,8 @@ def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, tem
     lane_status: int32 [lanes]; row_offsets: int32 [lanes + 1]; temperatures:
     float32 [lanes]; row_stats: int32 [rows, 8] from new_row_stats().
     ``rows`` defaults to target.shape[0] (it must equal row_offsets[-1]).
+    ``lane_base`` is the global index of lane 0 in the Philox counter (a batch
+    split into parts draws the uniforms of the unsplit batch).
     """
     lib = load_library()
     if target.dim() != 2 or target.stride(1) != 1 or target.dtype not in _DTYPES:
@@ -199,6 +202,7 @@ def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, tem
         out_tokens=out_tokens.data_ptr(),
         lane_status=None if lane_status is None else lane_status.data_ptr(),
         row_stats=None if row_stats is None else row_stats.data_ptr(),
+        lane_base=int(lane_base),
     )
     code = lib.spec_verify_accept(ctypes.byref(a), _stream(stream))
     if code != SPEC_OK:
@@ -211,7 +215,7 @@ def spec_verify_accept_raw(args, stream):
 
 
 def make_args(target, draft, draft_tokens, draft_lens, row_offsets, temperatures, seed,
-              committed, out_tokens, lane_status=None, row_stats=None, V=None, rows=None):
+              committed, out_tokens, lane_status=None, row_stats=None, V=None, rows=None, lane_base=0):
     """Build the C argument struct once (for tight loops that call it repeatedly)."""
     return _Args(
         target_logits=target.data_ptr(),
@@ -230,6 +234,7 @@ def make_args(target, draft, draft_tokens, draft_lens, row_offsets, temperatures
         out_tokens=out_tokens.data_ptr(),
         lane_status=None if lane_status is None else lane_status.data_ptr(),
         row_stats=None if row_stats is None else row_stats.data_ptr(),
+        lane_base=int(lane_base),
     )
 
 
@@ -261,22 +266,24 @@ def spec_commit_state(staged, live, committed, lane_status=None, stream=None):
         raise SpecError(code, "spec_commit_state")
 
 
-def spec_round_uniforms(seed, lanes, positions, device=None, stream=None):
+def spec_round_uniforms(seed, lanes, positions, lane_base=0, device=None, stream=None):
     """float32 [lanes, positions, 2]: the (u, u') pairs the verify kernel draws."""
     lib = load_library()
     device = device or torch.device("cuda", torch.cuda.current_device())
     out = torch.empty(lanes, positions, 2, dtype=torch.float32, device=device)
-    code = lib.spec_round_uniforms(int(seed) & ((1 << 64) - 1), int(lanes), int(positions),
+    code = lib.spec_round_uniforms(int(seed) & ((1 << 64) - 1), int(lane_base), int(lanes), int(positions),
                                    _ptr(out), _stream(stream))
     if code != SPEC_OK:
         raise SpecError(code, "spec_round_uniforms")
     return out
 
 
-def spec_verify_launch_shape(lanes, V, dtype=torch.bfloat16):
+def spec_verify_launch_shape(lanes, rows, V, dtype=torch.bfloat16):
+    """Launch shape spec_verify_accept would pick (see include/spec_verify.h)."""
     lib = load_library()
     vals = [ctypes.c_int32() for _ in range(4)]
-    code = lib.spec_verify_launch_shape(int(lanes), int(V), _DTYPES[dtype], *[ctypes.byref(v) for v in vals])
+    code = lib.spec_verify_launch_shape(int(lanes), int(rows), int(V), _DTYPES[dtype],
+                                        *[ctypes.byref(v) for v in vals])
     if code != SPEC_OK:
         raise SpecError(code, "spec_verify_launch_shape")
     return dict(zip(("cluster_ctas", "threads", "slice", "smem_bytes"), (v.value for v in vals)))

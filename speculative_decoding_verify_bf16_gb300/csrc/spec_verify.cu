@@ -64,16 +64,22 @@ struct VerifyShape {
 };
 
 // One cluster of `cluster` CTAs per lane; each CTA reduces `slice` elements of
-// every row of its lane.  Enough CTAs to fill the GPU about twice over, but
-// no fewer than 2048 elements per CTA.  The ring holds whole slices when they
-// fit in a 32 KB slot.
-VerifyShape choose_shape(int lanes, int V, int esize, bool aligned, int sms, int force_cluster) {
+// every row of its lane.  The cluster is the larger of (a) the smallest power
+// of two that gives about 1.5 CTAs per SM and (b) the smallest that keeps a
+// CTA's share of an average lane (rows / lanes rows, counted 1.5 times for
+// drafter rows of sampled lanes) at or below 512 KB; never fewer than 2048
+// elements per CTA.  The ring holds whole slices when they fit a 32 KB slot.
+VerifyShape choose_shape(int lanes, int rows, int V, int esize, bool aligned, int sms, int force_cluster) {
   VerifyShape s{};
   const int vec = 16 / esize;
   int C = force_cluster > 0 ? force_cluster : env_int("SPEC_VERIFY_CLUSTER", 0);
   if (C <= 0) {
-    C = 1;
-    while (C < specv::kMaxCluster && static_cast<int64_t>(lanes) * C < 2LL * sms) C *= 2;
+    int c_fill = 1;
+    while (c_fill < specv::kMaxCluster && static_cast<int64_t>(lanes) * c_fill * 2 < 3LL * sms) c_fill *= 2;
+    const double lane_bytes = 1.5 * rows / lanes * static_cast<double>(V) * esize;
+    int c_size = 1;
+    while (c_size < specv::kMaxCluster && lane_bytes / c_size > 512.0 * 1024) c_size *= 2;
+    C = c_fill > c_size ? c_fill : c_size;
     while (C > 1 && (V + C - 1) / C < 2048) C /= 2;
   }
   if (C > specv::kMaxCluster) C = specv::kMaxCluster;
@@ -158,12 +164,13 @@ bool cluster_fits(int dev, void* kernel, int cluster, int smem) {
   return ok;
 }
 
-__global__ void round_uniforms_kernel(uint64_t seed, int32_t lanes, int32_t positions, float* out) {
+__global__ void round_uniforms_kernel(uint64_t seed, uint32_t lane_base, int32_t lanes, int32_t positions,
+                                      float* out) {
   const int64_t total = static_cast<int64_t>(lanes) * positions;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int b = static_cast<int>(i / positions), j = static_cast<int>(i % positions);
-    const float2 u = specv::round_uniforms(seed, b, j);
+    const float2 u = specv::round_uniforms(seed, lane_base + static_cast<uint32_t>(b), j);
     out[2 * i] = u.x;
     out[2 * i + 1] = u.y;
   }
@@ -173,7 +180,8 @@ __global__ void round_uniforms_kernel(uint64_t seed, int32_t lanes, int32_t posi
 
 extern "C" {
 
-int spec_round_uniforms(uint64_t seed, int32_t lanes, int32_t positions, float* out, void* stream) {
+int spec_round_uniforms(uint64_t seed, uint32_t lane_base, int32_t lanes, int32_t positions, float* out,
+                        void* stream) {
   if (lanes < 0 || positions < 0) return SPEC_ERR_INVALID_ARG;
   const int64_t total = static_cast<int64_t>(lanes) * positions;
   if (total == 0) return SPEC_OK;
@@ -181,7 +189,7 @@ int spec_round_uniforms(uint64_t seed, int32_t lanes, int32_t positions, float* 
   int64_t blocks = (total + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   round_uniforms_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      seed, lanes, positions, out);
+      seed, lane_base, lanes, positions, out);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
@@ -209,12 +217,13 @@ const char* spec_status_string(int status) {
   }
 }
 
-int spec_verify_launch_shape(int32_t lanes, int32_t V, spec_dtype dtype, int32_t* cluster_ctas,
+int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype dtype, int32_t* cluster_ctas,
                              int32_t* threads, int32_t* slice, int32_t* smem_bytes) {
-  if (lanes <= 0 || V <= 0 || (dtype != SPEC_F32 && dtype != SPEC_BF16)) return SPEC_ERR_INVALID_ARG;
+  if (lanes <= 0 || rows < lanes || V <= 0 || (dtype != SPEC_F32 && dtype != SPEC_BF16))
+    return SPEC_ERR_INVALID_ARG;
   DeviceCache* dc = nullptr;
   if (device_cache(&dc, nullptr) != SPEC_OK) return SPEC_ERR_CUDA;
-  const VerifyShape s = choose_shape(lanes, V, dtype == SPEC_BF16 ? 2 : 4, true, dc->sms, 0);
+  const VerifyShape s = choose_shape(lanes, rows, V, dtype == SPEC_BF16 ? 2 : 4, true, dc->sms, 0);
   if (cluster_ctas) *cluster_ctas = s.cluster;
   if (threads) *threads = specv::kThreads;
   if (slice) *slice = s.slice;
@@ -240,7 +249,7 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
   const bool aligned = is_aligned16(a->target_logits) &&
                        (a->draft_logits == nullptr || is_aligned16(a->draft_logits)) &&
                        ((a->ld * esize) % 16 == 0);
-  VerifyShape s = choose_shape(a->lanes, a->V, esize, aligned, dc->sms, 0);
+  VerifyShape s = choose_shape(a->lanes, a->rows, a->V, esize, aligned, dc->sms, 0);
   if (s.smem > dc->smem_optin) return SPEC_ERR_UNSUPPORTED;
 
   void* kernel = pick_verify_kernel(a->dtype, aligned);
@@ -257,7 +266,7 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
   }
   // A cluster must fit into one GPU processing cluster; shrink it until one does.
   while (s.cluster > 1 && !cluster_fits(dev, kernel, s.cluster, s.smem))
-    s = choose_shape(a->lanes, a->V, esize, aligned, dc->sms, s.cluster / 2);
+    s = choose_shape(a->lanes, a->rows, a->V, esize, aligned, dc->sms, s.cluster / 2);
 
   specv::VerifyParams p{};
   p.target = static_cast<const uint8_t*>(a->target_logits);
@@ -275,6 +284,7 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
   p.out_tokens = a->out_tokens;
   p.lane_status = a->lane_status;
   p.row_stats = a->row_stats;
+  p.lane_base = a->lane_base;
   p.cluster = s.cluster;
   p.slice = s.slice;
   p.slot_bytes = s.slot_bytes;

@@ -110,6 +110,7 @@ struct VerifyParams {
   int32_t* out_tokens;
   int32_t* lane_status;
   spec_row_stats* row_stats;
+  uint32_t lane_base;  // global index of lane 0 in the Philox counter
   int32_t cluster;     // CTAs per lane
   int32_t slice;       // vocabulary elements per CTA (multiple of the vector width)
   int32_t slot_bytes;  // bytes per ring slot (multiple of 16)
@@ -609,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_accept_kernel(const Verify
         }
       }
       if (sampled) {
-        const float2 u = round_uniforms(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(j));
+        const float2 u = round_uniforms(p.seed, p.lane_base + static_cast<uint32_t>(b), static_cast<uint32_t>(j));
         sh.u_acc[j] = u.x;
         sh.u_smp[j] = u.y;
       }

@@ -68,7 +68,7 @@ def test_status_strings(lib):
 def test_calls_with_bad_arguments_fail_on_the_host(lib):
     # NULL argument struct and NULL out pointer: rejected before touching a GPU.
     assert lib.spec_verify_accept(None, None) == sv.SPEC_ERR_INVALID_ARG
-    assert lib.spec_round_uniforms(1, 4, 4, None, None) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_round_uniforms(1, 0, 4, 4, None, None) == sv.SPEC_ERR_INVALID_ARG
     assert lib.spec_commit_state(None, None, None, -1, 1, 16, 16, 16, 16, None, None) == \
         sv.SPEC_ERR_INVALID_ARG
     assert lib.spec_commit_state(None, None, None, 0, 1, 16, 16, 16, 16, None, None) == sv.SPEC_OK

@@ -109,8 +109,9 @@ def test_round_uniforms_match_the_oracle_generator():
             ua, us = oracle.round_uniforms(seed, b, j)
             assert u[b, j, 0] == ua and u[b, j, 1] == us, (b, j)
     # large lane ids and seeds exercise the high counter and key words
-    u = sv.spec_round_uniforms(2 ** 64 - 1, 3, 2).cpu().numpy()
-    assert u[2, 1, 0] == oracle.round_uniforms(2 ** 64 - 1, 2, 1)[0]
+    u = sv.spec_round_uniforms(2 ** 64 - 1, 3, 2, lane_base=2 ** 32 - 5).cpu().numpy()
+    assert u[2, 1, 0] == oracle.round_uniforms(2 ** 64 - 1, 2 ** 32 - 3, 1)[0]
+    assert u[2, 1, 1] == oracle.round_uniforms(2 ** 64 - 1, 2 ** 32 - 3, 1)[1]
 
 
 def test_greedy_equals_plain_argmax_decode_on_the_gpu():
@@ -311,3 +312,26 @@ def test_back_to_back_graph_launches_are_identical(monkeypatch, cluster, ring_kb
     compare(r, first, orc, check_stats=False)
     for o in outs[1:]:
         assert torch.equal(o[0], outs[0][0]) and torch.equal(o[1], outs[0][1]) and torch.equal(o[2], outs[0][2])
+
+
+def test_lane_shards_reproduce_the_unsplit_round():
+    """Verifying lanes [lo, hi) on their own with lane_base = lo gives exactly
+    the results those lanes get in the whole round (what a lane-sharded
+    multi-GPU run relies on)."""
+    from speculative_decoding_verify_bf16_gb300.sharding import lane_range, shard_rows
+
+    r = workloads.make_custom_round(91, DEV, lanes=11, vocab=50000, kmax=6, dtype="bf16", sampled="mixed")
+    full = run_gpu(r)
+    for rank in range(3):
+        lo, hi = lane_range(r.lanes, 3, rank)
+        row_lo, row_hi, offs = shard_rows(r.row_offsets.tolist(), lo, hi)
+        c = torch.zeros(hi - lo, dtype=torch.int32, device=DEV)
+        o = torch.zeros(row_hi - row_lo, dtype=torch.int32, device=DEV)
+        st = torch.zeros(hi - lo, dtype=torch.int32, device=DEV)
+        sv.spec_verify_accept(r.target[row_lo:row_hi], r.draft[row_lo:row_hi],
+                              r.draft_tokens[row_lo:row_hi].contiguous(), r.draft_lens[lo:hi].contiguous(),
+                              torch.tensor(offs, dtype=torch.int32, device=DEV),
+                              r.temperatures[lo:hi].contiguous(), r.seed, c, o, st, lane_base=lo)
+        torch.cuda.synchronize()
+        assert np.array_equal(c.cpu().numpy(), full["committed"][lo:hi])
+        assert np.array_equal(o.cpu().numpy(), full["out_tokens"][row_lo:row_hi])

@@ -151,11 +151,13 @@ def _per_row(values, lens, offsets):
     return torch.repeat_interleave(values, counts)
 
 
-def make_round(name, seed=0, device="cpu", with_state=True):
+def make_round(name, seed=0, device="cpu", with_state=True, commit_lanes=None):
     """Inputs of one named workload (see the module docstring).
 
     ``with_state=False`` skips the recurrent-state snapshots of the commit
     workload (callers that share one state between several logits sets).
+    ``commit_lanes`` shrinks the commit workload to fewer lanes (same shapes
+    per lane), for profiler captures that must stay small.
     """
     device = torch.device(device)
     g = _gen(seed, device)
@@ -173,11 +175,12 @@ def make_round(name, seed=0, device="cpu", with_state=True):
                               spike=8.0, alpha=None, dtype="bf16", temperature=0.7,
                               seed=philox_seed)
     if name == GREEDY_COMMIT_B64:
-        r = _fixed_k_round(name, g, device, lanes=64, k=3, vocab=151936, sigma=2.0,
+        lanes = 64 if commit_lanes is None else int(commit_lanes)
+        r = _fixed_k_round(name, g, device, lanes=lanes, k=3, vocab=151936, sigma=2.0,
                            spike=8.0, alpha=0.8, dtype="bf16", temperature=0.0,
                            seed=philox_seed)
         if with_state:
-            r.staged, r.live = make_state(64, 4, STATE_SHAPE, seed, device)
+            r.staged, r.live = make_state(lanes, 4, STATE_SHAPE, seed, device)
         return r
     if name == RAGGED_MIXED_B128:
         return _ragged_round(name, g, device, lanes=128, kmax=RAGGED_DRAFT_TOKENS,
