@@ -90,7 +90,9 @@ def profiled_traffic(kernel, workload):
     if fields.get("kernel_source_sha256") != kernel_source_hash():
         return None
     try:
-        return int(float(fields["dram_bytes_per_launch"]))
+        # A capture of a smaller case of the workload states the factor that
+        # scales its per-launch traffic to the full launch.
+        return int(float(fields["dram_bytes_per_launch"]) * float(fields.get("traffic_scale", "1")))
     except (KeyError, ValueError):
         return None
 
