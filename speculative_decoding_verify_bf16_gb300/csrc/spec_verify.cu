@@ -67,9 +67,11 @@ struct VerifyShape {
 // every row of its lane.  The cluster is the larger of (a) the smallest power
 // of two that gives about 1.5 CTAs per SM and (b) the smallest that keeps a
 // CTA's share of an average lane (rows / lanes rows, counted 1.5 times for
-// drafter rows of sampled lanes) at or below 512 KB; never fewer than 2048
-// elements per CTA.  The ring holds whole slices when they fit a 32 KB slot.
-VerifyShape choose_shape(int lanes, int rows, int V, int esize, bool aligned, int sms, int force_cluster) {
+// drafter rows of sampled lanes) at or below 1 MB; never fewer than 2048
+// elements per CTA.  The caller then shrinks it until clusters fit (see
+// spec_verify_accept).  The ring holds whole slices when they fit a 32 KB slot.
+VerifyShape choose_shape(int lanes, int rows, int V, int esize, bool aligned, int sms, int smem_optin,
+                         int force_cluster) {
   VerifyShape s{};
   const int vec = 16 / esize;
   int C = force_cluster > 0 ? force_cluster : env_int("SPEC_VERIFY_CLUSTER", 0);
@@ -78,7 +80,7 @@ VerifyShape choose_shape(int lanes, int rows, int V, int esize, bool aligned, in
     while (c_fill < specv::kMaxCluster && static_cast<int64_t>(lanes) * c_fill * 2 < 3LL * sms) c_fill *= 2;
     const double lane_bytes = 1.5 * rows / lanes * static_cast<double>(V) * esize;
     int c_size = 1;
-    while (c_size < specv::kMaxCluster && lane_bytes / c_size > 512.0 * 1024) c_size *= 2;
+    while (c_size < specv::kMaxCluster && lane_bytes / c_size > 1024.0 * 1024) c_size *= 2;
     C = c_fill > c_size ? c_fill : c_size;
     while (C > 1 && (V + C - 1) / C < 2048) C /= 2;
   }
@@ -96,9 +98,11 @@ VerifyShape choose_shape(int lanes, int rows, int V, int esize, bool aligned, in
   const int64_t slot_max = static_cast<int64_t>(env_int("SPEC_VERIFY_SLOT_KB", 32)) * 1024;
   const int64_t chunks = (slice_bytes + slot_max - 1) / slot_max;
   s.slot_bytes = static_cast<int>(round_up((slice_bytes + chunks - 1) / chunks, 16));
-  // 88 KB keeps two CTAs per SM possible, so that enough 16-CTA clusters can
-  // be resident at once.
-  const int64_t ring = static_cast<int64_t>(env_int("SPEC_VERIFY_RING_KB", 88)) * 1024;
+  // With 8 consumer warps 88 KB keeps two CTAs per SM possible; with 16 the
+  // CTA fills an SM and the ring takes all the shared memory left.
+  const int64_t ring_kb = env_int("SPEC_VERIFY_RING_KB", 0);
+  const int64_t ring = ring_kb > 0 ? ring_kb * 1024
+                                   : (specv::kConsumerWarps <= 8 ? 88 * 1024 : smem_optin - s.head_bytes);
   // A multiple of the kernel's consumer-warp groups (each group owns its slots).
   int nslots = static_cast<int>(ring / s.slot_bytes);
   nslots -= nslots % specv::kGroups;
@@ -123,27 +127,26 @@ void* pick_verify_kernel(int dtype, bool aligned) {
 
 bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Cluster sizes already found schedulable, per device / kernel / shared memory.
+// Clusters that can be resident at once, per device / kernel / cluster size /
+// shared memory (cached; cudaOccupancyMaxActiveClusters).
 struct ClusterFit {
   int dev;
   void* kernel;
   int smem;
   int cluster;
-  int fits;
+  int active;
 };
-constexpr int kFitCache = 64;
+constexpr int kFitCache = 128;
 ClusterFit g_fit[kFitCache];
 int g_fit_n = 0;
 
-// True if at least one cluster of `cluster` CTAs with `smem` bytes each can be
-// resident at once on this device.
-bool cluster_fits(int dev, void* kernel, int cluster, int smem) {
+int max_active_clusters(int dev, void* kernel, int cluster, int smem) {
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     for (int i = 0; i < g_fit_n; ++i)
       if (g_fit[i].dev == dev && g_fit[i].kernel == kernel && g_fit[i].smem == smem &&
           g_fit[i].cluster == cluster)
-        return g_fit[i].fits != 0;
+        return g_fit[i].active;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
@@ -157,11 +160,21 @@ bool cluster_fits(int dev, void* kernel, int cluster, int smem) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  const bool ok = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n > 0;
-  if (!ok) cudaGetLastError();
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_fit_n < kFitCache) g_fit[g_fit_n++] = ClusterFit{dev, kernel, smem, cluster, ok ? 1 : 0};
-  return ok;
+  if (g_fit_n < kFitCache) g_fit[g_fit_n++] = ClusterFit{dev, kernel, smem, cluster, n};
+  return n;
+}
+
+// The next smaller cluster size tried when one does not fit.
+int smaller_cluster(int c) {
+  static const int kSizes[] = {16, 12, 8, 6, 4, 2, 1};
+  for (int s : kSizes)
+    if (s < c) return s;
+  return 1;
 }
 
 __global__ void round_uniforms_kernel(uint64_t seed, uint32_t lane_base, int32_t lanes, int32_t positions,
@@ -223,7 +236,7 @@ int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype 
     return SPEC_ERR_INVALID_ARG;
   DeviceCache* dc = nullptr;
   if (device_cache(&dc, nullptr) != SPEC_OK) return SPEC_ERR_CUDA;
-  const VerifyShape s = choose_shape(lanes, rows, V, dtype == SPEC_BF16 ? 2 : 4, true, dc->sms, 0);
+  const VerifyShape s = choose_shape(lanes, rows, V, dtype == SPEC_BF16 ? 2 : 4, true, dc->sms, dc->smem_optin, 0);
   if (cluster_ctas) *cluster_ctas = s.cluster;
   if (threads) *threads = specv::kThreads;
   if (slice) *slice = s.slice;
@@ -249,7 +262,7 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
   const bool aligned = is_aligned16(a->target_logits) &&
                        (a->draft_logits == nullptr || is_aligned16(a->draft_logits)) &&
                        ((a->ld * esize) % 16 == 0);
-  VerifyShape s = choose_shape(a->lanes, a->rows, a->V, esize, aligned, dc->sms, 0);
+  VerifyShape s = choose_shape(a->lanes, a->rows, a->V, esize, aligned, dc->sms, dc->smem_optin, 0);
   if (s.smem > dc->smem_optin) return SPEC_ERR_UNSUPPORTED;
 
   void* kernel = pick_verify_kernel(a->dtype, aligned);
@@ -264,9 +277,18 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
       done = true;
     }
   }
-  // A cluster must fit into one GPU processing cluster; shrink it until one does.
-  while (s.cluster > 1 && !cluster_fits(dev, kernel, s.cluster, s.smem))
-    s = choose_shape(a->lanes, a->rows, a->V, esize, aligned, dc->sms, s.cluster / 2);
+  // A cluster must fit into one GPU processing cluster.  When every lane could
+  // run at once (few lanes) the cluster also shrinks until all of them fit
+  // together, so that no lane waits for a second wave.
+  {
+    const bool forced = env_int("SPEC_VERIFY_CLUSTER", 0) > 0;
+    for (;;) {
+      const int active = max_active_clusters(dev, kernel, s.cluster, s.smem);
+      const bool few = static_cast<int64_t>(a->lanes) * s.cluster <= 2LL * dc->sms;
+      if (s.cluster == 1 || (active > 0 && (forced || !few || active >= a->lanes))) break;
+      s = choose_shape(a->lanes, a->rows, a->V, esize, aligned, dc->sms, dc->smem_optin, smaller_cluster(s.cluster));
+    }
+  }
 
   specv::VerifyParams p{};
   p.target = static_cast<const uint8_t*>(a->target_logits);

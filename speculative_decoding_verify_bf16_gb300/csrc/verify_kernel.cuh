@@ -33,7 +33,12 @@ namespace specv {
 
 constexpr int kMaxDrafts = SPEC_MAX_DRAFTS;      // 15
 constexpr int kMaxStreams = 2 * kMaxDrafts + 1;  // target rows + drafter rows of one lane
-constexpr int kConsumerWarps = 8;
+// Consumer warps per CTA.  Sixteen give the latency hiding the sampled rows'
+// exponential sums need; the CTA then occupies a whole SM (one per SM).
+#ifndef SPEC_VERIFY_CONSUMER_WARPS
+#define SPEC_VERIFY_CONSUMER_WARPS 16
+#endif
+constexpr int kConsumerWarps = SPEC_VERIFY_CONSUMER_WARPS;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps;    // streams the slices (lane 0)
 constexpr int kHelperWarp = kConsumerWarps + 1;  // draft tokens, logits at them, uniforms
@@ -51,7 +56,6 @@ constexpr int kGroups = kConsumerWarps / kPieces;
 static_assert(kConsumerWarps % kPieces == 0, "consumer warps must form whole groups");
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr double kLog2eD = 1.4426950408889634;
 constexpr double kLn2d = 0.6931471805599453;
 
 // Partial reduction of one row over some elements (16 bytes, pushed over DSMEM).
@@ -162,6 +166,12 @@ __device__ __forceinline__ void acc_init(Acc& a) {
   a.nan2 = 0xFF80FF80u;  // (-inf, -inf)
 }
 
+// Sums of sampled rows are kept relative to the scaled reference fl(m * c)
+// of the running max m (c = log2(e) / T): s = sum 2^(x * c - fl(m * c)).
+// Each term is then one FMA and one exp2, and the reference can always be
+// recomputed from m, so merges rescale by 2^(fl(m_i * c) - fl(M * c)).
+__device__ __forceinline__ float scaled_ref(float m, float c) { return __fmul_rn(m, c); }
+
 // Merge (m2, s2, i2) into (m, s, idx): max, rescaled sum, lowest index of the max.
 template <bool SAMPLED>
 __device__ __forceinline__ void merge_part(float& m, float& s, int& idx, float m2, float s2, int i2,
@@ -171,7 +181,8 @@ __device__ __forceinline__ void merge_part(float& m, float& s, int& idx, float m
     if (nm == -INFINITY) {
       s = s + s2;
     } else {
-      s = s * ex2_approx((m - nm) * c) + s2 * ex2_approx((m2 - nm) * c);
+      const float rn = scaled_ref(nm, c);
+      s = s * ex2_approx(scaled_ref(m, c) - rn) + s2 * ex2_approx(scaled_ref(m2, c) - rn);
     }
   }
   if (m2 > m || (m2 == m && i2 < idx)) idx = i2;
@@ -181,60 +192,14 @@ __device__ __forceinline__ void merge_part(float& m, float& s, int& idx, float m
 // A new running max `vm` first seen at element `e`: rescale the sum.
 template <bool SAMPLED>
 __device__ __forceinline__ void acc_raise(Acc& a, float vm, int e, float c) {
-  if (SAMPLED) a.s *= ex2_approx((a.m - vm) * c);
+  if (SAMPLED) a.s *= ex2_approx(scaled_ref(a.m, c) - scaled_ref(vm, c));
   a.m = vm;
   a.idx = e;
 }
 
-__device__ __forceinline__ float exp_term(float x, float mm, float c) {
-  return ex2_approx((x - mm) * c);
-}
-
-// 8 bf16 logits starting at element e0.
-template <bool SAMPLED>
-__device__ __forceinline__ void acc_bf16x8(Acc& a, const uint4 v, int e0, float c) {
-  const uint32_t h = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
-  a.nan2 = bf16x2_max_nan(a.nan2, h);
-  const float vm = fmaxf(bf16_lo(h), bf16_hi(h));
-  if (vm > a.m) {
-    const float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                        bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-    int i = 0;
-#pragma unroll
-    for (int t = 7; t >= 0; --t)
-      if (x[t] == vm) i = t;
-    acc_raise<SAMPLED>(a, vm, e0 + i, c);
-  }
-  if (SAMPLED) {
-    const float mm = (a.m == -INFINITY) ? 0.f : a.m;
-    const float e01 = exp_term(bf16_lo(v.x), mm, c) + exp_term(bf16_hi(v.x), mm, c);
-    const float e23 = exp_term(bf16_lo(v.y), mm, c) + exp_term(bf16_hi(v.y), mm, c);
-    const float e45 = exp_term(bf16_lo(v.z), mm, c) + exp_term(bf16_hi(v.z), mm, c);
-    const float e67 = exp_term(bf16_lo(v.w), mm, c) + exp_term(bf16_hi(v.w), mm, c);
-    a.s += (e01 + e23) + (e45 + e67);
-  }
-}
-
-// 4 fp32 logits starting at element e0.
-template <bool SAMPLED>
-__device__ __forceinline__ void acc_f32x4(Acc& a, const uint4 v, int e0, float c) {
-  const float x[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                      __uint_as_float(v.w)};
-#pragma unroll
-  for (int t = 0; t < 4; ++t) a.bad |= !(x[t] <= FLT_MAX);
-  const float vm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-  if (vm > a.m) {
-    int i = 0;
-#pragma unroll
-    for (int t = 3; t >= 0; --t)
-      if (x[t] == vm) i = t;
-    acc_raise<SAMPLED>(a, vm, e0 + i, c);
-  }
-  if (SAMPLED) {
-    const float mm = (a.m == -INFINITY) ? 0.f : a.m;
-    a.s += (exp_term(x[0], mm, c) + exp_term(x[1], mm, c)) +
-           (exp_term(x[2], mm, c) + exp_term(x[3], mm, c));
-  }
+// 2^(x * c - mr): one FMA and one exp2 (mr = the scaled reference).
+__device__ __forceinline__ float exp_term(float x, float mr, float c) {
+  return ex2_approx(fmaf(x, c, -mr));
 }
 
 // One logit (row tails and unaligned rows).
@@ -243,17 +208,8 @@ __device__ __forceinline__ void acc_scalar(Acc& a, float x, int e, float c) {
   a.bad |= !(x <= FLT_MAX);
   if (x > a.m) acc_raise<SAMPLED>(a, x, e, c);
   if (SAMPLED) {
-    const float mm = (a.m == -INFINITY) ? 0.f : a.m;
-    a.s += exp_term(x, mm, c);
-  }
-}
-
-template <typename T, bool SAMPLED>
-__device__ __forceinline__ void acc_vec(Acc& a, const uint4 v, int e0, float c) {
-  if constexpr (ElemTraits<T>::kVec == 8) {
-    acc_bf16x8<SAMPLED>(a, v, e0, c);
-  } else {
-    acc_f32x4<SAMPLED>(a, v, e0, c);
+    const float mr = (a.m == -INFINITY) ? 0.f : scaled_ref(a.m, c);
+    a.s += exp_term(x, mr, c);
   }
 }
 
@@ -296,39 +252,123 @@ __device__ __forceinline__ float vec_exp_sum(const uint4 v, float mm, float c) {
   }
 }
 
+template <typename T>
+__device__ __forceinline__ uint4 neg_inf_vec() {
+  if constexpr (ElemTraits<T>::kVec == 8) return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+  else return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+}
+
+// Vector v of the piece, or -inf everywhere past its end (no exponential
+// weight, never a maximum).
+template <typename T>
+__device__ __forceinline__ uint4 vec_or_neg_inf(const uint4* sv, int v, int ve) {
+  return (v < ve) ? sv[v] : neg_inf_vec<T>();
+}
+
 // One piece of a chunk in shared memory, processed by one warp: this lane's
-// vectors are vb + lane, vb + lane + 32, ... below ve.  Phase 1 keeps the
-// largest vector maximum and the first vector holding it, with two independent
-// accumulators so that consecutive vectors do not wait on each other; the
-// lowest element index is then looked up in that one vector, and only if it
-// beats the running max.  Phase 2 (sampled rows) sums the exponentials at the
-// now fixed max with four independent partial sums.
-template <typename T, bool SAMPLED>
-__device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int ve, int ebase, float c,
-                                          int lane) {
+// vectors are vb + lane, vb + lane + 32, ... below ve, four at a time; past
+// the piece they read as -inf (no exponential weight, never a maximum), so the
+// loops stay four wide to the end instead of finishing in a serial tail.
+// Phase 1 keeps the largest vector maximum and the first vector holding it in
+// two independent accumulators (vectors 0, 2 and 1, 3 of each group; each
+// still sees its vectors in increasing order); the lowest element index is
+// then looked up in that one vector, and only if it beats the running max.
+// Phase 2 (sampled rows) sums the exponentials at the now fixed max with four
+// independent partial sums.
+// Sampled rows, one pass: each group of four vectors (32 elements per lane)
+// is summed relative to its own maximum, so a group's exponentials depend only
+// on its own registers and consecutive groups overlap; group sums then join
+// the piece's running sum with one rescaling exp2 per group.  The argmax is
+// kept as in the greedy phase 1.
+template <typename T>
+__device__ __forceinline__ void acc_range_sampled(Acc& a, const uint4* sv, int vb, int ve, int ebase, float c,
+                                                  int lane) {
   constexpr int kVec = ElemTraits<T>::kVec;
   float m0 = -INFINITY, m1 = -INFINITY, nanacc = -INFINITY;
   int i0 = INT_MAX, i1 = INT_MAX;
-  int v = vb + lane;
-  for (; v + 32 < ve; v += 64) {
-    const float a0 = vec_max_nan<T>(sv[v]);
-    const float a1 = vec_max_nan<T>(sv[v + 32]);
-    nanacc = f32_max_nan(nanacc, f32_max_nan(a0, a1));
-    if (a0 > m0) {
-      m0 = a0;
+  float M = -INFINITY, S = 0.f;  // piece max and sum relative to scaled_ref(M)
+#pragma unroll 2
+  for (int v = vb + lane; v < ve; v += 128) {
+    uint4 x[4];
+    float vm[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      x[u] = vec_or_neg_inf<T>(sv, v + 32 * u, ve);
+      vm[u] = vec_max_nan<T>(x[u]);
+    }
+    if (vm[0] > m0) {
+      m0 = vm[0];
       i0 = v;
     }
-    if (a1 > m1) {
-      m1 = a1;
+    if (vm[1] > m1) {
+      m1 = vm[1];
       i1 = v + 32;
     }
+    if (vm[2] > m0) {
+      m0 = vm[2];
+      i0 = v + 64;
+    }
+    if (vm[3] > m1) {
+      m1 = vm[3];
+      i1 = v + 96;
+    }
+    const float gm = f32_max_nan(f32_max_nan(vm[0], vm[1]), f32_max_nan(vm[2], vm[3]));
+    nanacc = f32_max_nan(nanacc, gm);
+    if (gm == -INFINITY) continue;  // nothing but -inf (or padding) in this group
+    const float rg = scaled_ref(gm, c);
+    const float sg = (vec_exp_sum<T>(x[0], rg, c) + vec_exp_sum<T>(x[1], rg, c)) +
+                     (vec_exp_sum<T>(x[2], rg, c) + vec_exp_sum<T>(x[3], rg, c));
+    if (gm > M) {
+      S = (M == -INFINITY) ? sg : fmaf(S, ex2_approx(scaled_ref(M, c) - rg), sg);
+      M = gm;
+    } else {
+      S = fmaf(sg, ex2_approx(rg - scaled_ref(M, c)), S);
+    }
   }
-  if (v < ve) {
-    const float a0 = vec_max_nan<T>(sv[v]);
-    nanacc = f32_max_nan(nanacc, a0);
-    if (a0 > m0) {
-      m0 = a0;
+  if (nanacc != nanacc || nanacc == INFINITY) a.bad = 1;
+  if (m1 > m0 || (m1 == m0 && i1 < i0)) {
+    m0 = m1;
+    i0 = i1;
+  }
+  if (m0 == -INFINITY) return;
+  int e = 0;
+  const uint4 xv = sv[i0];
+#pragma unroll
+  for (int t = kVec - 1; t >= 0; --t)
+    if (vec_elem<T>(xv, t) == m0) e = t;
+  merge_part<true>(a.m, a.s, a.idx, M, S, ebase + i0 * kVec + e, c);
+}
+
+template <typename T, bool SAMPLED>
+__device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int ve, int ebase, float c,
+                                          int lane) {
+  if constexpr (SAMPLED) {
+    acc_range_sampled<T>(a, sv, vb, ve, ebase, c, lane);
+    return;
+  }
+  constexpr int kVec = ElemTraits<T>::kVec;
+  float m0 = -INFINITY, m1 = -INFINITY, nanacc = -INFINITY;
+  int i0 = INT_MAX, i1 = INT_MAX;
+  for (int v = vb + lane; v < ve; v += 128) {
+    float a4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) a4[u] = vec_max_nan<T>(vec_or_neg_inf<T>(sv, v + 32 * u, ve));
+    nanacc = f32_max_nan(nanacc, f32_max_nan(f32_max_nan(a4[0], a4[1]), f32_max_nan(a4[2], a4[3])));
+    if (a4[0] > m0) {
+      m0 = a4[0];
       i0 = v;
+    }
+    if (a4[1] > m1) {
+      m1 = a4[1];
+      i1 = v + 32;
+    }
+    if (a4[2] > m0) {
+      m0 = a4[2];
+      i0 = v + 64;
+    }
+    if (a4[3] > m1) {
+      m1 = a4[3];
+      i1 = v + 96;
     }
   }
   if (nanacc != nanacc || nanacc == INFINITY) a.bad = 1;
@@ -345,16 +385,14 @@ __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int v
     acc_raise<SAMPLED>(a, m0, ebase + i0 * kVec + e, c);
   }
   if (SAMPLED) {
-    const float mm = (a.m == -INFINITY) ? 0.f : a.m;
+    const float mm = (a.m == -INFINITY) ? 0.f : scaled_ref(a.m, c);
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    int w = vb + lane;
-    for (; w + 96 < ve; w += 128) {
-      s0 += vec_exp_sum<T>(sv[w], mm, c);
-      s1 += vec_exp_sum<T>(sv[w + 32], mm, c);
-      s2 += vec_exp_sum<T>(sv[w + 64], mm, c);
-      s3 += vec_exp_sum<T>(sv[w + 96], mm, c);
+    for (int w = vb + lane; w < ve; w += 128) {
+      s0 += vec_exp_sum<T>(vec_or_neg_inf<T>(sv, w, ve), mm, c);
+      s1 += vec_exp_sum<T>(vec_or_neg_inf<T>(sv, w + 32, ve), mm, c);
+      s2 += vec_exp_sum<T>(vec_or_neg_inf<T>(sv, w + 64, ve), mm, c);
+      s3 += vec_exp_sum<T>(vec_or_neg_inf<T>(sv, w + 96, ve), mm, c);
     }
-    for (; w < ve; w += 32) s0 += vec_exp_sum<T>(sv[w], mm, c);
     a.s += (s0 + s1) + (s2 + s3);
   }
 }
@@ -375,7 +413,7 @@ __device__ __forceinline__ Partial warp_merge(float m, float s, int idx, uint32_
   const float M = warp_max_f32(m);
   const int I = __reduce_min_sync(0xFFFFFFFFu, (m == M) ? idx : INT_MAX);
   if (SAMPLED) {
-    float t = (M == -INFINITY) ? s : s * ex2_approx((m - M) * c);
+    float t = (M == -INFINITY) ? s : s * ex2_approx(scaled_ref(m, c) - scaled_ref(M, c));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
     s = t;
@@ -389,16 +427,16 @@ __device__ __forceinline__ Partial identity_partial() { return Partial{-INFINITY
 // Pass-2 draw weights
 // ---------------------------------------------------------------------------
 struct DrawCoef {
-  float mp, l2sp;  // target row: max and log2 of its sum
+  float mp, l2sp;  // target row: scaled reference fl(max * c) and log2 of its sum
   float mq, l2sq;  // drafter row (residual only)
   float c;         // log2(e) / T
   bool residual;
 };
 
-// Normalised probability 2^((x - m) * c - log2 S), evaluated with explicit
-// roundings so that both call sites produce identical bits.
-__device__ __forceinline__ float prob_at(float x, float m, float l2s, float c) {
-  return ex2_approx(__fmaf_rn(__fsub_rn(x, m), c, -l2s));
+// Normalised probability 2^(x * c - fl(m * c) - log2 S), evaluated with
+// explicit roundings so that both call sites produce identical bits.
+__device__ __forceinline__ float prob_at(float x, float mr, float l2s, float c) {
+  return ex2_approx(__fsub_rn(__fmaf_rn(x, c, -mr), l2s));
 }
 
 __device__ __forceinline__ float draw_weight(const DrawCoef& k, float xt, float xq) {
@@ -408,50 +446,63 @@ __device__ __forceinline__ float draw_weight(const DrawCoef& k, float xt, float 
   return fmaxf(0.f, __fsub_rn(p, q));
 }
 
-// Eight consecutive logits of a row from element e (values past `end` read as -inf).
+// Eight consecutive logits of a row, kept as raw bits (one 16-byte vector of
+// bf16, two of fp32) so that several rounds can be in flight at once.
+template <typename T>
+struct Raw8 {
+  uint4 v[ElemTraits<T>::kVec == 8 ? 1 : 2];
+};
+
+template <typename T>
+__device__ __forceinline__ float raw_elem(const Raw8<T>& r, int i) {
+  if constexpr (ElemTraits<T>::kVec == 8) return vec_elem<T>(r.v[0], i);
+  else return vec_elem<T>(r.v[i >> 2], i & 3);
+}
+
+// Elements e .. e+7 of a row; those at or past `end` read as -inf.
 template <typename T, bool ALIGNED>
-__device__ __forceinline__ void load8(const uint8_t* row, int e, int end, float (&x)[8]) {
+__device__ __forceinline__ void load_raw8(const uint8_t* row, int e, int end, Raw8<T>& r) {
+  constexpr bool kBf16 = ElemTraits<T>::kVec == 8;
   if (ALIGNED && e + 8 <= end) {
-    if constexpr (ElemTraits<T>::kVec == 8) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + static_cast<int64_t>(e) * 2));
-      x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
-      x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
-    } else {
-      const uint4* p = reinterpret_cast<const uint4*>(row + static_cast<int64_t>(e) * 4);
-      const uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
-      x[0] = __uint_as_float(v0.x); x[1] = __uint_as_float(v0.y);
-      x[2] = __uint_as_float(v0.z); x[3] = __uint_as_float(v0.w);
-      x[4] = __uint_as_float(v1.x); x[5] = __uint_as_float(v1.y);
-      x[6] = __uint_as_float(v1.z); x[7] = __uint_as_float(v1.w);
-    }
+    const uint4* p = reinterpret_cast<const uint4*>(row + static_cast<int64_t>(e) * (kBf16 ? 2 : 4));
+    r.v[0] = __ldg(p);
+    if constexpr (!kBf16) r.v[1] = __ldg(p + 1);
   } else {
+    uint32_t w[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = (e + i < end) ? ElemTraits<T>::load(row, e + i) : -INFINITY;
+    for (int i = 0; i < 8; ++i) {
+      if constexpr (kBf16) {
+        w[i] = (e + i < end) ? static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(row) + e + i))
+                             : 0xFF80u;
+      } else {
+        w[i] = (e + i < end) ? __float_as_uint(__ldg(reinterpret_cast<const float*>(row) + e + i))
+                             : 0xFF800000u;
+      }
+    }
+    if constexpr (kBf16) {
+      r.v[0] = make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16), w[6] | (w[7] << 16));
+    } else {
+      r.v[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      r.v[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
   }
 }
 
 // The eight draw weights of one lane's piece of a pass-2 round, and their
 // running sums in element order (cum[7] is the piece's total).
-template <typename T, bool ALIGNED>
-__device__ __forceinline__ void draw_piece(const DrawCoef& k, const uint8_t* trow,
-                                           const uint8_t* qrow, int e, int end, float (&w)[8],
-                                           float (&cum)[8]) {
-  float xt[8], xq[8];
-  load8<T, ALIGNED>(trow, e, end, xt);
-  if (k.residual) {
-    load8<T, ALIGNED>(qrow, e, end, xq);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) xq[i] = -INFINITY;
-  }
+template <typename T>
+__device__ __forceinline__ void draw_piece(const DrawCoef& k, const Raw8<T>& rt, const Raw8<T>& rq, int e,
+                                           int end, float (&w)[8], float (&cum)[8]) {
   float run = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    w[i] = (e + i < end) ? draw_weight(k, xt[i], xq[i]) : 0.f;
+    w[i] = (e + i < end) ? draw_weight(k, raw_elem<T>(rt, i), k.residual ? raw_elem<T>(rq, i) : -INFINITY) : 0.f;
     run = __fadd_rn(run, w[i]);
     cum[i] = run;
   }
 }
+
+constexpr int kDrawBatch = 4;  // pass-2 rounds whose loads are issued together
 
 __device__ __forceinline__ float warp_sum_xor(float v) {
 #pragma unroll
@@ -490,7 +541,7 @@ __device__ __forceinline__ void push_partials(SmemHead& sh, int nstreams, int C,
 }
 
 template <typename T, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads, 1) verify_accept_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_accept_kernel(const VerifyParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SmemHead& sh = *reinterpret_cast<SmemHead*>(smem_raw);
   uint8_t* ring = smem_raw + p.head_bytes;
@@ -746,10 +797,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_accept_kernel(const Verify
     }
 
     int n = 0, mode = kNoDraw;
-    // log2 p_j(d) and log2 q_j(d) at this lane's position:
-    //   (x_d - max) * log2(e) / T - log2(S)
-    // The difference x_d - max is exact, the rest is done in fp64 from an
-    // fp64 1/T and an accurate log2 of S, so they carry ~1e-7 absolute error.
+    // log2 p_j(d) and log2 q_j(d) at this lane's position, in the terms the
+    // sums were taken in:  x_d * c - fl(max * c) - log2(S).  x_d * c is exact
+    // in fp64 and log2(S) is accurate to ~1e-7, so both carry ~1e-7 error.
     double lp = NAN, lq = NAN;
     if (st == SPEC_OK) {
       const bool active = lane < k;
@@ -760,10 +810,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_accept_kernel(const Verify
       } else {
         bool accept = true;
         if (active) {
-          const double c64 = kLog2eD / static_cast<double>(temp);
+          const double cd = static_cast<double>(c);
           const Partial pt = sh.fin[2 * lane], pq = sh.fin[2 * lane + 1];
-          lp = static_cast<double>(sh.xd_t[lane] - pt.m) * c64 - log2_split(pt.s);
-          lq = static_cast<double>(sh.xd_q[lane] - pq.m) * c64 - log2_split(pq.s);
+          lp = (static_cast<double>(sh.xd_t[lane]) * cd - static_cast<double>(scaled_ref(pt.m, c))) -
+               log2_split(pt.s);
+          lq = (static_cast<double>(sh.xd_q[lane]) * cd - static_cast<double>(scaled_ref(pq.m, c))) -
+               log2_split(pq.s);
           if (lp == -INFINITY) accept = false;
           else if (lq == -INFINITY) accept = true;
           else accept = log2_split(sh.u_acc[lane]) < lp - lq;
@@ -800,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_accept_kernel(const Verify
           rs->argmax = pt.idx;
           rs->max_logit = pt.m;
           if (sampled) {
-            rs->lse = static_cast<float>(static_cast<double>(pt.m) / temp + log2_split(pt.s) * kLn2d);
+            rs->lse = static_cast<float>((static_cast<double>(scaled_ref(pt.m, c)) + log2_split(pt.s)) * kLn2d);
             rs->logp_d = (j < k) ? static_cast<float>(lp * kLn2d) : NAN;
             rs->logq_d = (j < k) ? static_cast<float>(lq * kLn2d) : NAN;
           } else {
@@ -829,7 +881,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_accept_kernel(const Verify
   auto make_coef = [&]() {
     DrawCoef kc;
     const Partial pt = sh.fin[2 * draw_row];
-    kc.mp = pt.m;
+    kc.mp = scaled_ref(pt.m, c);
     kc.l2sp = log2f(pt.s);
     kc.c = c;
     kc.residual = residual;
@@ -837,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_accept_kernel(const Verify
     kc.l2sq = 0.f;
     if (residual) {
       const Partial pq = sh.fin[2 * n + 1];
-      kc.mq = pq.m;
+      kc.mq = scaled_ref(pq.m, c);
       kc.l2sq = log2f(pq.s);
     }
     return kc;
@@ -855,14 +907,27 @@ __global__ void __launch_bounds__(kThreads, 1) verify_accept_kernel(const Verify
       const int s1 = min(v1, s0 + seg);
       float segw = 0.f;
       int last = -1;
-      for (int base = s0; base < s1; base += kDrawRound) {
-        float w[8], cum[8];
-        const int e = base + lane * 8;
-        draw_piece<T, ALIGNED>(kc, trow, qrow, e, s1, w, cum);
+      for (int base = s0; base < s1; base += kDrawBatch * kDrawRound) {
+        Raw8<T> rt[kDrawBatch], rq[kDrawBatch];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (w[i] > 0.f) last = e + i;
-        segw = __fadd_rn(segw, warp_sum_xor(cum[7]));
+        for (int u = 0; u < kDrawBatch; ++u) {
+          const int e = base + u * kDrawRound + lane * 8;
+          if (base + u * kDrawRound < s1) {
+            load_raw8<T, ALIGNED>(trow, e, s1, rt[u]);
+            if (kc.residual) load_raw8<T, ALIGNED>(qrow, e, s1, rq[u]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kDrawBatch; ++u) {
+          if (base + u * kDrawRound >= s1) break;
+          float w[8], cum[8];
+          const int e = base + u * kDrawRound + lane * 8;
+          draw_piece<T>(kc, rt[u], rq[u], e, s1, w, cum);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (w[i] > 0.f) last = e + i;
+          segw = __fadd_rn(segw, warp_sum_xor(cum[7]));
+        }
       }
       last = warp_max_int(last);
       if (lane == 0) {
@@ -948,10 +1013,23 @@ __global__ void __launch_bounds__(kThreads, 1) verify_accept_kernel(const Verify
       const int s1 = min(v1, s0 + seg);
       float run = 0.f;
       int found = -1;
-      for (int base = s0; base < s1 && found < 0; base += kDrawRound) {
+      for (int bbase = s0; bbase < s1 && found < 0; bbase += kDrawBatch * kDrawRound) {
+        Raw8<T> rt[kDrawBatch], rq[kDrawBatch];
+#pragma unroll
+        for (int u = 0; u < kDrawBatch; ++u) {
+          const int e = bbase + u * kDrawRound + lane * 8;
+          if (bbase + u * kDrawRound < s1) {
+            load_raw8<T, ALIGNED>(trow, e, s1, rt[u]);
+            if (kc.residual) load_raw8<T, ALIGNED>(qrow, e, s1, rq[u]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kDrawBatch; ++u) {
+        const int base = bbase + u * kDrawRound;
+        if (base >= s1 || found >= 0) break;
         float w[8], cum[8];
         const int e = base + lane * 8;
-        draw_piece<T, ALIGNED>(kc, trow, qrow, e, s1, w, cum);
+        draw_piece<T>(kc, rt[u], rq[u], e, s1, w, cum);
         const float R = warp_sum_xor(cum[7]);
         const float next = __fadd_rn(run, R);
         if (next > tau1) {
@@ -990,6 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_accept_kernel(const Verify
           found = tok;
         }
         run = next;
+        }
       }
       if (found < 0) found = sh.seglast[warp];
       if (lane == 0) {
