@@ -80,8 +80,9 @@ enum DrawMode : int { kNoDraw = 0, kResidual = 1, kBonus = 2 };
 struct __align__(16) SmemHead {
   uint64_t full[kMaxSlots];
   uint64_t empty[kMaxSlots];
-  uint64_t xbar;     // completes when every peer's row partials have landed
+  uint64_t xbar;     // completes when every peer's row partials (or keys) have landed
   uint64_t dbar[2];  // the same for the pass-2 slice sums
+  unsigned long long gkey[kMaxDrafts + 1];     // greedy lanes: this CTA's argmax key of every row
   Partial wpart[kMaxStreams][kConsumerWarps];  // per consumer warp
   Partial cpart[kMaxCluster][kMaxStreams];     // per CTA of the cluster (pushed by peers)
   Partial fin[kMaxStreams];                    // this CTA's partial, then the lane's total
@@ -423,6 +424,39 @@ __device__ __forceinline__ Partial warp_merge(float m, float s, int idx, uint32_
 
 __device__ __forceinline__ Partial identity_partial() { return Partial{-INFINITY, 0.f, INT_MAX, 0u}; }
 
+// Greedy rows reduce to one 64-bit key per row: the order-preserving bits of
+// the max on top and the complemented index below, so that the largest key is
+// the largest logit at its lowest index and partial results combine with a
+// single atomic max.  -0 is folded into +0 first (the two compare equal, so
+// the lower index must win between them).  0 means "no element".
+__device__ __forceinline__ unsigned long long argmax_key(float m, int idx) {
+  if (idx == INT_MAX) return 0ull;
+  uint32_t u = __float_as_uint(__fadd_rn(m, 0.f));
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(idx));
+}
+
+__device__ __forceinline__ void argmax_key_decode(unsigned long long key, float& m, int& idx) {
+  if (key == 0ull) {
+    m = -INFINITY;
+    idx = INT_MAX;
+    return;
+  }
+  const uint32_t u = static_cast<uint32_t>(key >> 32);
+  m = __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+  idx = static_cast<int>(~static_cast<uint32_t>(key));
+}
+
+// A consumer warp's contribution to greedy row s: the warp's max and lowest
+// index of it, folded into the CTA's key of the row; flags go straight into
+// the CTA's flag word.
+__device__ __forceinline__ void fold_greedy_row(SmemHead& sh, int s, float m, int idx, uint32_t flags, int lane) {
+  const float M = warp_max_f32(m);
+  const int I = __reduce_min_sync(0xFFFFFFFFu, (m == M) ? idx : INT_MAX);
+  if (flags) atomicOr(&sh.cta_flags, flags);
+  if (lane == 0 && I != INT_MAX) atomicMax(&sh.gkey[s], argmax_key(M, I));
+}
+
 // ---------------------------------------------------------------------------
 // Pass-2 draw weights
 // ---------------------------------------------------------------------------
@@ -502,7 +536,12 @@ __device__ __forceinline__ void draw_piece(const DrawCoef& k, const Raw8<T>& rt,
   }
 }
 
-constexpr int kDrawBatch = 4;  // pass-2 rounds whose loads are issued together
+// Pass-2 rounds whose loads are issued together (fp32 rounds hold twice the
+// registers).
+template <typename T>
+__host__ __device__ constexpr int draw_batch() {
+  return ElemTraits<T>::kVec == 8 ? 4 : 2;
+}
 
 __device__ __forceinline__ float warp_sum_xor(float v) {
 #pragma unroll
@@ -520,13 +559,12 @@ __device__ __forceinline__ int warp_max_int(int v) {
 // The kernel
 // ---------------------------------------------------------------------------
 
-// Push this CTA's partial of every row into the CTAs that need it: the leader
-// only for greedy lanes, every CTA of the cluster for sampled lanes.  A peer's
-// copy goes by st.async and completes the receiver's xbar; the CTA's own copy
-// is a plain shared-memory store.
+// Push this CTA's partial of every row of a sampled lane into every CTA of
+// the cluster.  A peer's copy goes by st.async and completes the receiver's
+// xbar; the CTA's own copy is a plain shared-memory store.
 __device__ __forceinline__ void push_partials(SmemHead& sh, int nstreams, int C, uint32_t rank,
-                                              bool to_all, uint32_t extra_flags) {
-  const int dests = to_all ? C : 1;
+                                              uint32_t extra_flags) {
+  const int dests = C;
   for (int t = threadIdx.x; t < nstreams * dests; t += kThreads) {
     const int s = t / dests, dst = t % dests;
     const Partial q = sh.fin[s];
@@ -536,6 +574,49 @@ __device__ __forceinline__ void push_partials(SmemHead& sh, int nstreams, int C,
     } else {
       st_async_v4(cluster_map(&sh.cpart[rank][s], dst), __float_as_uint(q.m), __float_as_uint(q.s),
                   static_cast<uint32_t>(q.idx), fl, cluster_map(&sh.xbar, dst));
+    }
+  }
+}
+
+// Acceptance scan and outputs of a greedy lane, run by one warp that holds
+// the lane's combined keys: lane j has the key of row j and `flags` is the
+// OR of every CTA's flags.  Draft d_{j+1} is accepted while it equals the
+// argmax of row j; the committed tokens are the argmaxes of rows 0..n.
+__device__ __forceinline__ void greedy_finish(const VerifyParams& p, const SmemHead& sh, int b, int k, int off,
+                                              int status, unsigned long long key, uint32_t flags, int lane) {
+  float m;
+  int a;
+  argmax_key_decode(key, m, a);
+  int st = status;
+  const bool range_bad = (st == SPEC_OK) && lane < k && (sh.drafts[lane] < 0 || sh.drafts[lane] >= p.V);
+  const bool empty_row = (st == SPEC_OK) && lane <= k && key == 0ull;
+  const bool any_range_bad = __any_sync(0xFFFFFFFFu, range_bad);
+  const bool any_empty = __any_sync(0xFFFFFFFFu, empty_row);
+  if (st == SPEC_OK) {
+    if (any_range_bad) st = SPEC_ERR_TOKEN_RANGE;
+    else if (flags & kTimedOut) st = SPEC_ERR_TIMEOUT;
+    else if ((flags & kBadValue) || any_empty) st = SPEC_ERR_NONFINITE;
+  }
+  const bool stop = (st == SPEC_OK) && lane < k && sh.drafts[lane] != a;
+  const uint32_t mask = __ballot_sync(0xFFFFFFFFu, stop);
+  const int n = mask ? (__ffs(mask) - 1) : k;
+  if (lane == 0) {
+    p.committed[b] = (st == SPEC_OK) ? n + 1 : 0;
+    if (p.lane_status) p.lane_status[b] = st;
+  }
+  if (status == SPEC_ERR_LAYOUT) return;
+  for (int j = lane; j <= k; j += 32) {
+    p.out_tokens[off + j] = (st == SPEC_OK && j <= n) ? a : -1;
+    if (p.row_stats && st == SPEC_OK) {
+      spec_row_stats* rs = p.row_stats + off + j;
+      rs->argmax = a;
+      rs->max_logit = m;
+      rs->lse = NAN;
+      rs->logp_d = NAN;
+      rs->logq_d = NAN;
+      rs->resid_mass = NAN;
+      rs->drawn = -1;
+      rs->flags = 1;
     }
   }
 }
@@ -569,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     sh.cta_flags = 0;
     fence_mbar_init();
   }
+  if (tid <= kMaxDrafts) sh.gkey[tid] = 0ull;
   griddep_wait();
 
   // ---- lane metadata (read by every thread; one transaction per warp) ----
@@ -587,6 +669,11 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   }
   const int nstreams = (status != SPEC_OK) ? 0 : (sampled ? 2 * k + 1 : k + 1);
   const float c = sampled ? __fdiv_rn(kLog2e, temp) : 0.f;
+  // Let the next kernel on the stream start its set-up now.  It cannot begin
+  // before every CTA of this grid has started and issued this, and it reads
+  // nothing of ours before its own griddepcontrol.wait, which waits for this
+  // whole grid to finish; issuing it late costs ~0.7 us at the end instead.
+  if (tid == 0) griddep_launch_dependents();
 
   const int v0 = min(p.V, static_cast<int>(rank) * p.slice);
   const int v1 = min(p.V, v0 + p.slice);
@@ -599,6 +686,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   // (leader of a greedy lane, or every CTA of a sampled lane), then for
   // sampled lanes their pass-2 slice sums.  Announced before this CTA arrives
   // on the cluster barrier, so before any peer can push.
+  // (A greedy lane's peers send 16 bytes per row to the leader only.)
   if (tid == 0) {
     const bool receives = sampled || leader;
     mbar_arrive_expect_tx(&sh.xbar, receives ? static_cast<uint32_t>((C - 1) * nstreams * 16) : 0u);
@@ -671,8 +759,9 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     // sequence is split into kPieces ranges of vectors, and warp w takes items
     // w, w + 8, ...  Warps therefore work on different chunks at once and only
     // meet at the end.  A warp merges its lanes only when its row changes.
-    for (int s = 0; s < nstreams; ++s)
-      if (lane == 0) sh.wpart[s][warp] = identity_partial();
+    if (sampled)
+      for (int s = 0; s < nstreams; ++s)
+        if (lane == 0) sh.wpart[s][warp] = identity_partial();
     bool ok = true;
     if (ALIGNED && body > 0) {
       const int nch = (body + slot_elems - 1) / slot_elems;  // chunks per row
@@ -685,9 +774,12 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
         const int s = ch / nch, ci = ch % nch;
         if (s != cur) {
           if (cur >= 0) {
-            const Partial wp = sampled ? warp_merge<true>(a.m, a.s, a.idx, acc_bad(a), c)
-                                       : warp_merge<false>(a.m, a.s, a.idx, acc_bad(a), c);
-            if (lane == 0) sh.wpart[cur][warp] = wp;
+            if (sampled) {
+              const Partial wp = warp_merge<true>(a.m, a.s, a.idx, acc_bad(a), c);
+              if (lane == 0) sh.wpart[cur][warp] = wp;
+            } else {
+              fold_greedy_row(sh, cur, a.m, a.idx, acc_bad(a), lane);
+            }
           }
           acc_init(a);
           cur = s;
@@ -710,9 +802,12 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       }
       if (cur >= 0) {
         const uint32_t fl = acc_bad(a) | (ok ? 0u : kTimedOut);
-        const Partial wp = sampled ? warp_merge<true>(a.m, a.s, a.idx, fl, c)
-                                   : warp_merge<false>(a.m, a.s, a.idx, fl, c);
-        if (lane == 0) sh.wpart[cur][warp] = wp;
+        if (sampled) {
+          const Partial wp = warp_merge<true>(a.m, a.s, a.idx, fl, c);
+          if (lane == 0) sh.wpart[cur][warp] = wp;
+        } else {
+          fold_greedy_row(sh, cur, a.m, a.idx, fl, lane);
+        }
       }
     }
     // Elements outside the bulk-copied body: the row tail, or the whole slice
@@ -728,35 +823,65 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
           if (sampled) acc_scalar<true>(a, x, v0 + e, c);
           else acc_scalar<false>(a, x, v0 + e, c);
         }
-        const Partial wp = sampled ? warp_merge<true>(a.m, a.s, a.idx, acc_bad(a), c)
-                                   : warp_merge<false>(a.m, a.s, a.idx, acc_bad(a), c);
-        if (lane == 0) {
-          Partial o = sh.wpart[s][warp];
-          if (sampled) merge_part<true>(o.m, o.s, o.idx, wp.m, wp.s, wp.idx, c);
-          else merge_part<false>(o.m, o.s, o.idx, wp.m, wp.s, wp.idx, c);
-          o.flags |= wp.flags;
-          sh.wpart[s][warp] = o;
+        if (sampled) {
+          const Partial wp = warp_merge<true>(a.m, a.s, a.idx, acc_bad(a), c);
+          if (lane == 0) {
+            Partial o = sh.wpart[s][warp];
+            merge_part<true>(o.m, o.s, o.idx, wp.m, wp.s, wp.idx, c);
+            o.flags |= wp.flags;
+            sh.wpart[s][warp] = o;
+          }
+        } else {
+          fold_greedy_row(sh, s, a.m, a.idx, acc_bad(a), lane);
         }
       }
     }
     if (!ok && lane == 0) atomicOr(&sh.cta_flags, kTimedOut);
   }
   __syncthreads();
-  griddep_launch_dependents();
 
-  // ---- this CTA's partial of every row ----
+  // ---- greedy lanes: the leader gathers every CTA's row keys and finishes ----
+  if (!sampled) {
+    cluster_wait_acquire();  // every peer is running: its shared memory may be written
+    if (warp != 0) return;
+    const uint32_t fl = sh.cta_flags;
+    if (!leader) {
+      // Lane s sends this CTA's key of row s, with the CTA's flags, into
+      // the leader's slot of this CTA.
+      if (lane < nstreams) {
+        const unsigned long long key = sh.gkey[lane];
+        st_async_v4(cluster_map(&sh.cpart[rank][lane], 0), static_cast<uint32_t>(key),
+                    static_cast<uint32_t>(key >> 32), fl, 0u, cluster_map(&sh.xbar, 0));
+      }
+      return;
+    }
+    const bool waited = mbar_wait_bounded(&sh.xbar, 0);
+    unsigned long long key = 0ull;
+    uint32_t flags = fl | (waited ? 0u : kTimedOut);
+    if (lane < nstreams) {
+      key = sh.gkey[lane];
+      for (int r = 1; r < C; ++r) {
+        const uint4 e = *reinterpret_cast<const uint4*>(&sh.cpart[r][lane]);
+        const unsigned long long kr = (static_cast<unsigned long long>(e.y) << 32) | e.x;
+        key = kr > key ? kr : key;
+        flags |= e.z;
+      }
+    }
+    greedy_finish(p, sh, b, k, off, status, key, __reduce_or_sync(0xFFFFFFFFu, flags), lane);
+    return;
+  }
+
+  // ---- sampled lanes: this CTA's partial of every row ----
   if (warp < kConsumerWarps) {
     for (int s = warp; s < nstreams; s += kConsumerWarps) {
       const Partial q = (lane < kConsumerWarps) ? sh.wpart[s][lane] : identity_partial();
-      const Partial r = sampled ? warp_merge<true>(q.m, q.s, q.idx, q.flags, c)
-                                : warp_merge<false>(q.m, q.s, q.idx, q.flags, c);
+      const Partial r = warp_merge<true>(q.m, q.s, q.idx, q.flags, c);
       if (lane == 0) sh.fin[s] = r;
     }
   }
   __syncthreads();
   cluster_wait_acquire();  // every peer is running: its shared memory may be written
-  push_partials(sh, nstreams, C, rank, sampled, sh.cta_flags);
-  if (!sampled && !leader) return;  // greedy lanes: the leader finishes alone
+  push_partials(sh, nstreams, C, rank, sh.cta_flags);
 
   // ---- the lane's totals ----
   if (tid == 0 && !mbar_wait_bounded(&sh.xbar, 0)) atomicOr(&sh.cta_flags, kTimedOut);
@@ -764,8 +889,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   if (warp < kConsumerWarps) {
     for (int s = warp; s < nstreams; s += kConsumerWarps) {
       const Partial q = (lane < C) ? sh.cpart[lane][s] : identity_partial();
-      const Partial r = sampled ? warp_merge<true>(q.m, q.s, q.idx, q.flags, c)
-                                : warp_merge<false>(q.m, q.s, q.idx, q.flags, c);
+      const Partial r = warp_merge<true>(q.m, q.s, q.idx, q.flags, c);
       if (lane == 0) sh.fin[s] = r;
     }
   }
@@ -803,28 +927,21 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     double lp = NAN, lq = NAN;
     if (st == SPEC_OK) {
       const bool active = lane < k;
-      bool stop;
-      if (!sampled) {
-        const int a = (lane <= k) ? sh.fin[lane].idx : 0;
-        stop = active && (sh.drafts[lane] != a);
-      } else {
-        bool accept = true;
-        if (active) {
-          const double cd = static_cast<double>(c);
-          const Partial pt = sh.fin[2 * lane], pq = sh.fin[2 * lane + 1];
-          lp = (static_cast<double>(sh.xd_t[lane]) * cd - static_cast<double>(scaled_ref(pt.m, c))) -
-               log2_split(pt.s);
-          lq = (static_cast<double>(sh.xd_q[lane]) * cd - static_cast<double>(scaled_ref(pq.m, c))) -
-               log2_split(pq.s);
-          if (lp == -INFINITY) accept = false;
-          else if (lq == -INFINITY) accept = true;
-          else accept = log2_split(sh.u_acc[lane]) < lp - lq;
-        }
-        stop = active && !accept;
+      bool accept = true;
+      if (active) {
+        const double cd = static_cast<double>(c);
+        const Partial pt = sh.fin[2 * lane], pq = sh.fin[2 * lane + 1];
+        lp = (static_cast<double>(sh.xd_t[lane]) * cd - static_cast<double>(scaled_ref(pt.m, c))) -
+             log2_split(pt.s);
+        lq = (static_cast<double>(sh.xd_q[lane]) * cd - static_cast<double>(scaled_ref(pq.m, c))) -
+             log2_split(pq.s);
+        if (lp == -INFINITY) accept = false;
+        else if (lq == -INFINITY) accept = true;
+        else accept = log2_split(sh.u_acc[lane]) < lp - lq;
       }
-      const uint32_t mask = __ballot_sync(0xFFFFFFFFu, stop);
+      const uint32_t mask = __ballot_sync(0xFFFFFFFFu, active && !accept);
       n = mask ? (__ffs(mask) - 1) : k;
-      if (sampled) mode = (n < k) ? kResidual : kBonus;
+      mode = (n < k) ? kResidual : kBonus;
     }
     if (lane == 0) {
       sh.scan_n = n;
@@ -839,27 +956,17 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
         if (p.lane_status) p.lane_status[b] = st;
       }
       for (int j = lane; layout_ok && j <= k; j += 32) {
-        int tok = -1;
-        if (st == SPEC_OK) {
-          if (!sampled) tok = (j <= n) ? sh.fin[j].idx : -1;
-          else tok = (j < n) ? sh.drafts[j] : -1;
-        }
-        const bool drawn_here = (st == SPEC_OK) && sampled && j == n;
+        const int tok = (st == SPEC_OK && j < n) ? sh.drafts[j] : -1;
+        const bool drawn_here = (st == SPEC_OK) && j == n;
         if (!drawn_here) p.out_tokens[off + j] = tok;
         if (p.row_stats && st == SPEC_OK) {
           spec_row_stats* rs = p.row_stats + off + j;
-          const Partial pt = sh.fin[sampled ? 2 * j : j];
+          const Partial pt = sh.fin[2 * j];
           rs->argmax = pt.idx;
           rs->max_logit = pt.m;
-          if (sampled) {
-            rs->lse = static_cast<float>((static_cast<double>(scaled_ref(pt.m, c)) + log2_split(pt.s)) * kLn2d);
-            rs->logp_d = (j < k) ? static_cast<float>(lp * kLn2d) : NAN;
-            rs->logq_d = (j < k) ? static_cast<float>(lq * kLn2d) : NAN;
-          } else {
-            rs->lse = NAN;
-            rs->logp_d = NAN;
-            rs->logq_d = NAN;
-          }
+          rs->lse = static_cast<float>((static_cast<double>(scaled_ref(pt.m, c)) + log2_split(pt.s)) * kLn2d);
+          rs->logp_d = (j < k) ? static_cast<float>(lp * kLn2d) : NAN;
+          rs->logq_d = (j < k) ? static_cast<float>(lq * kLn2d) : NAN;
           if (!(drawn_here && mode == kResidual)) rs->resid_mass = NAN;
           if (!drawn_here) rs->drawn = -1;
           rs->flags = 1 | (drawn_here ? (mode == kResidual ? 2 : 4) : 0);
@@ -869,9 +976,10 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   }
   __syncthreads();
 
-  if (!sampled || sh.scan_mode == kNoDraw) return;
+  if (sh.scan_mode == kNoDraw) return;
 
   // ---- pass 2: draw the model's token (sampled lanes, whole cluster) ----
+  constexpr int kDrawBatch = draw_batch<T>();
   const int n = sh.scan_n;
   bool residual = (sh.scan_mode == kResidual);
   int draw_row = residual ? n : k;  // target row whose p enters the weights
