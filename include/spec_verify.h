@@ -198,10 +198,10 @@ const char* spec_status_string(int status);
  * Host-only.  Reports the CTAs per lane (one thread-block cluster per lane),
  * threads per CTA, the vocabulary slice each CTA reduces, and the dynamic shared
  * memory per CTA, for a verify over `lanes` lanes and `rows` rows of vocabulary
- * V in `dtype` with 16-byte aligned rows on the current device, before any
- * reduction of the cluster that the device's scheduling limits may force.
- * Any output pointer may be NULL.  Returns SPEC_OK, SPEC_ERR_INVALID_ARG or
- * SPEC_ERR_CUDA.
+ * V in `dtype` with 16-byte aligned rows on the current device, after the
+ * cluster has been shrunk to what the device can schedule (the same rule the
+ * launch applies).  Any output pointer may be NULL.  Returns SPEC_OK,
+ * SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED or SPEC_ERR_CUDA.
  */
 int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype dtype, int32_t* cluster_ctas,
                              int32_t* threads, int32_t* slice, int32_t* smem_bytes);

@@ -189,6 +189,39 @@ __global__ void round_uniforms_kernel(uint64_t seed, uint32_t lane_base, int32_t
   }
 }
 
+// The shape spec_verify_accept launches: choose_shape, then, since a cluster
+// must fit into one GPU processing cluster, smaller clusters until one fits.
+// When every lane could run at once (few lanes) the cluster also shrinks until
+// all of them fit together, so that no lane waits for a second wave.
+int resolve_shape(DeviceCache* dc, int dev, int lanes, int rows, int V, int dtype, bool aligned, VerifyShape* out,
+                  void** kernel_out) {
+  const int esize = (dtype == SPEC_BF16) ? 2 : 4;
+  VerifyShape s = choose_shape(lanes, rows, V, esize, aligned, dc->sms, dc->smem_optin, 0);
+  if (s.smem > dc->smem_optin) return SPEC_ERR_UNSUPPORTED;
+  void* kernel = pick_verify_kernel(dtype, aligned);
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    bool& done = dc->verify_attr[kernel_index(dtype, aligned)];
+    if (!done) {
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dc->smem_optin) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+      done = true;
+    }
+  }
+  const bool forced = env_int("SPEC_VERIFY_CLUSTER", 0) > 0;
+  for (;;) {
+    const int active = max_active_clusters(dev, kernel, s.cluster, s.smem);
+    const bool few = static_cast<int64_t>(lanes) * s.cluster <= 2LL * dc->sms;
+    if (s.cluster == 1 || (active > 0 && (forced || !few || active >= lanes))) break;
+    s = choose_shape(lanes, rows, V, esize, aligned, dc->sms, dc->smem_optin, smaller_cluster(s.cluster));
+  }
+  *out = s;
+  if (kernel_out) *kernel_out = kernel;
+  return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -235,8 +268,11 @@ int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype 
   if (lanes <= 0 || rows < lanes || V <= 0 || (dtype != SPEC_F32 && dtype != SPEC_BF16))
     return SPEC_ERR_INVALID_ARG;
   DeviceCache* dc = nullptr;
-  if (device_cache(&dc, nullptr) != SPEC_OK) return SPEC_ERR_CUDA;
-  const VerifyShape s = choose_shape(lanes, rows, V, dtype == SPEC_BF16 ? 2 : 4, true, dc->sms, dc->smem_optin, 0);
+  int dev = 0;
+  if (device_cache(&dc, &dev) != SPEC_OK) return SPEC_ERR_CUDA;
+  VerifyShape s{};
+  const int rc = resolve_shape(dc, dev, lanes, rows, V, dtype, true, &s, nullptr);
+  if (rc != SPEC_OK) return rc;
   if (cluster_ctas) *cluster_ctas = s.cluster;
   if (threads) *threads = specv::kThreads;
   if (slice) *slice = s.slice;
@@ -262,33 +298,10 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
   const bool aligned = is_aligned16(a->target_logits) &&
                        (a->draft_logits == nullptr || is_aligned16(a->draft_logits)) &&
                        ((a->ld * esize) % 16 == 0);
-  VerifyShape s = choose_shape(a->lanes, a->rows, a->V, esize, aligned, dc->sms, dc->smem_optin, 0);
-  if (s.smem > dc->smem_optin) return SPEC_ERR_UNSUPPORTED;
-
-  void* kernel = pick_verify_kernel(a->dtype, aligned);
-  {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    bool& done = dc->verify_attr[kernel_index(a->dtype, aligned)];
-    if (!done) {
-      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dc->smem_optin) !=
-              cudaSuccess ||
-          cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-        return SPEC_ERR_CUDA;
-      done = true;
-    }
-  }
-  // A cluster must fit into one GPU processing cluster.  When every lane could
-  // run at once (few lanes) the cluster also shrinks until all of them fit
-  // together, so that no lane waits for a second wave.
-  {
-    const bool forced = env_int("SPEC_VERIFY_CLUSTER", 0) > 0;
-    for (;;) {
-      const int active = max_active_clusters(dev, kernel, s.cluster, s.smem);
-      const bool few = static_cast<int64_t>(a->lanes) * s.cluster <= 2LL * dc->sms;
-      if (s.cluster == 1 || (active > 0 && (forced || !few || active >= a->lanes))) break;
-      s = choose_shape(a->lanes, a->rows, a->V, esize, aligned, dc->sms, dc->smem_optin, smaller_cluster(s.cluster));
-    }
-  }
+  VerifyShape s{};
+  void* kernel = nullptr;
+  const int rc = resolve_shape(dc, dev, a->lanes, a->rows, a->V, a->dtype, aligned, &s, &kernel);
+  if (rc != SPEC_OK) return rc;
 
   specv::VerifyParams p{};
   p.target = static_cast<const uint8_t*>(a->target_logits);

@@ -44,9 +44,12 @@ constexpr int kProducerWarp = kConsumerWarps;    // streams the slices (lane 0)
 constexpr int kHelperWarp = kConsumerWarps + 1;  // draft tokens, logits at them, uniforms
 constexpr int kThreads = kConsumers + 64;
 constexpr int kMaxCluster = 16;
-constexpr int kMaxSlots = 16;
+constexpr int kMaxSlots = 32;
 constexpr int kDrawRound = 256;  // elements per warp per pass-2 round (32 lanes x 8)
-constexpr int kPieces = 4;       // warps sharing one chunk of the ring
+#ifndef SPEC_VERIFY_PIECES
+#define SPEC_VERIFY_PIECES 4
+#endif
+constexpr int kPieces = SPEC_VERIFY_PIECES;  // warps sharing one chunk of the ring
 // Consumer warps form kGroups groups of kPieces; group g takes the chunks
 // ch = g (mod kGroups).  The ring must have a multiple of kGroups slots so
 // that every slot belongs to one group: a warp then only ever waits on a slot
@@ -226,31 +229,59 @@ __device__ __forceinline__ float vec_elem(const uint4 v, int e) {
   }
 }
 
-// Largest element of one vector, NaN if any element is NaN.
-template <typename T>
-__device__ __forceinline__ float vec_max_nan(const uint4 v) {
-  if constexpr (ElemTraits<T>::kVec == 8) {
-    const uint32_t h = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
-    return f32_max_nan(bf16_lo(h), bf16_hi(h));
-  } else {
-    return f32_max_nan(f32_max_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
-                       f32_max_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
-  }
+// Packed pairs of fp32 (the f32x2 forms of FMA and add issue both halves as
+// one instruction).
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
 }
 
-// Sum of 2^((x - mm) * c) over the elements of one vector.
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// 2^z of both halves.
+__device__ __forceinline__ unsigned long long f2_ex2(unsigned long long z) {
+  float lo, hi;
+  f2_unpack(z, lo, hi);
+  return f2_pack(ex2_approx(lo), ex2_approx(hi));
+}
+
+// The two elements of one 32-bit word of a vector as a packed fp32 pair
+// (bf16: the low and high halves widened; fp32 vectors give pairs of words).
+__device__ __forceinline__ unsigned long long bf16_pair(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// acc + sum over the vector's elements of 2^(x * c - mr), as packed pairs;
+// c2 = (c, c), nmr2 = (-mr, -mr).
 template <typename T>
-__device__ __forceinline__ float vec_exp_sum(const uint4 v, float mm, float c) {
+__device__ __forceinline__ unsigned long long vec_exp_acc(const uint4 v, unsigned long long c2,
+                                                          unsigned long long nmr2, unsigned long long acc) {
   if constexpr (ElemTraits<T>::kVec == 8) {
-    const float e01 = exp_term(bf16_lo(v.x), mm, c) + exp_term(bf16_hi(v.x), mm, c);
-    const float e23 = exp_term(bf16_lo(v.y), mm, c) + exp_term(bf16_hi(v.y), mm, c);
-    const float e45 = exp_term(bf16_lo(v.z), mm, c) + exp_term(bf16_hi(v.z), mm, c);
-    const float e67 = exp_term(bf16_lo(v.w), mm, c) + exp_term(bf16_hi(v.w), mm, c);
-    return (e01 + e23) + (e45 + e67);
+    acc = f2_add(acc, f2_ex2(f2_fma(bf16_pair(v.x), c2, nmr2)));
+    acc = f2_add(acc, f2_ex2(f2_fma(bf16_pair(v.y), c2, nmr2)));
+    acc = f2_add(acc, f2_ex2(f2_fma(bf16_pair(v.z), c2, nmr2)));
+    acc = f2_add(acc, f2_ex2(f2_fma(bf16_pair(v.w), c2, nmr2)));
   } else {
-    return (exp_term(__uint_as_float(v.x), mm, c) + exp_term(__uint_as_float(v.y), mm, c)) +
-           (exp_term(__uint_as_float(v.z), mm, c) + exp_term(__uint_as_float(v.w), mm, c));
+    acc = f2_add(acc, f2_ex2(f2_fma(f2_pack(__uint_as_float(v.x), __uint_as_float(v.y)), c2, nmr2)));
+    acc = f2_add(acc, f2_ex2(f2_fma(f2_pack(__uint_as_float(v.z), __uint_as_float(v.w)), c2, nmr2)));
   }
+  return acc;
 }
 
 template <typename T>
@@ -259,142 +290,121 @@ __device__ __forceinline__ uint4 neg_inf_vec() {
   else return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
 }
 
-// Vector v of the piece, or -inf everywhere past its end (no exponential
-// weight, never a maximum).
+// The four vectors v, v + 32, v + 64, v + 96 of one lane's group; with PRED,
+// those at or past ve read as -inf (no exponential weight, never a maximum).
+template <typename T, bool PRED>
+__device__ __forceinline__ void load_group(const uint4* sv, int v, int ve, uint4 (&x)[4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) x[u] = (!PRED || v + 32 * u < ve) ? sv[v + 32 * u] : neg_inf_vec<T>();
+}
+
+// Per-vector maxima of a group, still packed (bf16: a bf16 pair per vector;
+// fp32: the vector's max), NaN-propagating.
 template <typename T>
-__device__ __forceinline__ uint4 vec_or_neg_inf(const uint4* sv, int v, int ve) {
-  return (v < ve) ? sv[v] : neg_inf_vec<T>();
+__device__ __forceinline__ void group_vec_max(const uint4 (&x)[4], uint32_t (&h)[4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    if constexpr (ElemTraits<T>::kVec == 8) {
+      h[u] = bf16x2_max_nan(bf16x2_max_nan(x[u].x, x[u].y), bf16x2_max_nan(x[u].z, x[u].w));
+    } else {
+      h[u] = __float_as_uint(f32_max_nan(f32_max_nan(__uint_as_float(x[u].x), __uint_as_float(x[u].y)),
+                                         f32_max_nan(__uint_as_float(x[u].z), __uint_as_float(x[u].w))));
+    }
+  }
+}
+
+// Widen one packed per-vector max to fp32.
+template <typename T>
+__device__ __forceinline__ float unpack_max(uint32_t h) {
+  if constexpr (ElemTraits<T>::kVec == 8) return f32_max_nan(bf16_lo(h), bf16_hi(h));
+  else return __uint_as_float(h);
+}
+
+// Largest element of the group from its per-vector maxima.
+template <typename T>
+__device__ __forceinline__ float group_max_nan(const uint32_t (&h)[4]) {
+  if constexpr (ElemTraits<T>::kVec == 8) {
+    return unpack_max<T>(bf16x2_max_nan(bf16x2_max_nan(h[0], h[1]), bf16x2_max_nan(h[2], h[3])));
+  } else {
+    return f32_max_nan(f32_max_nan(__uint_as_float(h[0]), __uint_as_float(h[1])),
+                       f32_max_nan(__uint_as_float(h[2]), __uint_as_float(h[3])));
+  }
+}
+
+// Lowest element index of vector vv holding m (the vector is known to hold it).
+template <typename T>
+__device__ __forceinline__ int vec_find(const uint4* sv, int vv, float m) {
+  constexpr int kVec = ElemTraits<T>::kVec;
+  const uint4 xv = sv[vv];
+  int e = 0;
+#pragma unroll
+  for (int t = kVec - 1; t >= 0; --t)
+    if (vec_elem<T>(xv, t) == m) e = t;
+  return vv * kVec + e;
 }
 
 // One piece of a chunk in shared memory, processed by one warp: this lane's
-// vectors are vb + lane, vb + lane + 32, ... below ve, four at a time; past
-// the piece they read as -inf (no exponential weight, never a maximum), so the
-// loops stay four wide to the end instead of finishing in a serial tail.
-// Phase 1 keeps the largest vector maximum and the first vector holding it in
-// two independent accumulators (vectors 0, 2 and 1, 3 of each group; each
-// still sees its vectors in increasing order); the lowest element index is
-// then looked up in that one vector, and only if it beats the running max.
-// Phase 2 (sampled rows) sums the exponentials at the now fixed max with four
-// independent partial sums.
-// Sampled rows, one pass: each group of four vectors (32 elements per lane)
-// is summed relative to its own maximum, so a group's exponentials depend only
-// on its own registers and consecutive groups overlap; group sums then join
-// the piece's running sum with one rescaling exp2 per group.  The argmax is
-// kept as in the greedy phase 1.
-template <typename T>
-__device__ __forceinline__ void acc_range_sampled(Acc& a, const uint4* sv, int vb, int ve, int ebase, float c,
-                                                  int lane) {
-  constexpr int kVec = ElemTraits<T>::kVec;
-  float m0 = -INFINITY, m1 = -INFINITY, nanacc = -INFINITY;
-  int i0 = INT_MAX, i1 = INT_MAX;
-  float M = -INFINITY, S = 0.f;  // piece max and sum relative to scaled_ref(M)
-#pragma unroll 2
-  for (int v = vb + lane; v < ve; v += 128) {
-    uint4 x[4];
-    float vm[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      x[u] = vec_or_neg_inf<T>(sv, v + 32 * u, ve);
-      vm[u] = vec_max_nan<T>(x[u]);
-    }
-    if (vm[0] > m0) {
-      m0 = vm[0];
-      i0 = v;
-    }
-    if (vm[1] > m1) {
-      m1 = vm[1];
-      i1 = v + 32;
-    }
-    if (vm[2] > m0) {
-      m0 = vm[2];
-      i0 = v + 64;
-    }
-    if (vm[3] > m1) {
-      m1 = vm[3];
-      i1 = v + 96;
-    }
-    const float gm = f32_max_nan(f32_max_nan(vm[0], vm[1]), f32_max_nan(vm[2], vm[3]));
-    nanacc = f32_max_nan(nanacc, gm);
-    if (gm == -INFINITY) continue;  // nothing but -inf (or padding) in this group
-    const float rg = scaled_ref(gm, c);
-    const float sg = (vec_exp_sum<T>(x[0], rg, c) + vec_exp_sum<T>(x[1], rg, c)) +
-                     (vec_exp_sum<T>(x[2], rg, c) + vec_exp_sum<T>(x[3], rg, c));
-    if (gm > M) {
-      S = (M == -INFINITY) ? sg : fmaf(S, ex2_approx(scaled_ref(M, c) - rg), sg);
-      M = gm;
-    } else {
-      S = fmaf(sg, ex2_approx(rg - scaled_ref(M, c)), S);
-    }
-  }
-  if (nanacc != nanacc || nanacc == INFINITY) a.bad = 1;
-  if (m1 > m0 || (m1 == m0 && i1 < i0)) {
-    m0 = m1;
-    i0 = i1;
-  }
-  if (m0 == -INFINITY) return;
-  int e = 0;
-  const uint4 xv = sv[i0];
-#pragma unroll
-  for (int t = kVec - 1; t >= 0; --t)
-    if (vec_elem<T>(xv, t) == m0) e = t;
-  merge_part<true>(a.m, a.s, a.idx, M, S, ebase + i0 * kVec + e, c);
-}
-
+// vectors are vb + lane, vb + lane + 32, ... below ve, taken four at a time
+// as groups (only the last group of the piece is predicated).  Each group's
+// max (NaN-propagating, so that NaN and +inf are flagged) is computed once;
+// a lane keeps its running max and the first group that reached it, and the
+// element index is looked up in that group after the piece.  Sampled rows
+// also sum each group's exponentials relative to the group's own max
+// (fl(max * c) as reference, packed fp32 pairs), and fold the group sum into
+// the lane's running sum with one rescaling exp2.
 template <typename T, bool SAMPLED>
 __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int ve, int ebase, float c,
                                           int lane) {
-  if constexpr (SAMPLED) {
-    acc_range_sampled<T>(a, sv, vb, ve, ebase, c, lane);
-    return;
-  }
-  constexpr int kVec = ElemTraits<T>::kVec;
-  float m0 = -INFINITY, m1 = -INFINITY, nanacc = -INFINITY;
-  int i0 = INT_MAX, i1 = INT_MAX;
-  for (int v = vb + lane; v < ve; v += 128) {
-    float a4[4];
+  float M = -INFINITY, nanacc = -INFINITY;
+  float S = 0.f;  // sampled: sum relative to scaled_ref(M)
+  int gv = -1;    // first vector holding M
+  const unsigned long long c2 = f2_pack(c, c);
+  auto group = [&](const uint4 (&x)[4], int v) {
+    uint32_t h[4];
+    group_vec_max<T>(x, h);
+    const float gm = group_max_nan<T>(h);
+    nanacc = f32_max_nan(nanacc, gm);
+    if (SAMPLED && gm != -INFINITY) {
+      const float rg = scaled_ref(gm, c);
+      const unsigned long long nmr2 = f2_pack(-rg, -rg);
+      unsigned long long acc = 0ull;  // (+0, +0)
 #pragma unroll
-    for (int u = 0; u < 4; ++u) a4[u] = vec_max_nan<T>(vec_or_neg_inf<T>(sv, v + 32 * u, ve));
-    nanacc = f32_max_nan(nanacc, f32_max_nan(f32_max_nan(a4[0], a4[1]), f32_max_nan(a4[2], a4[3])));
-    if (a4[0] > m0) {
-      m0 = a4[0];
-      i0 = v;
+      for (int u = 0; u < 4; ++u) acc = vec_exp_acc<T>(x[u], c2, nmr2, acc);
+      float lo, hi;
+      f2_unpack(acc, lo, hi);
+      const float sg = lo + hi;
+      if (gm > M) S = (M == -INFINITY) ? sg : fmaf(S, ex2_approx(scaled_ref(M, c) - rg), sg);
+      else S = fmaf(sg, ex2_approx(rg - scaled_ref(M, c)), S);
     }
-    if (a4[1] > m1) {
-      m1 = a4[1];
-      i1 = v + 32;
+    if (gm > M) {
+      // A new running max (rare after the first groups): the first vector of
+      // the group that holds it.
+      M = gm;
+      gv = v + 96;
+#pragma unroll
+      for (int u = 2; u >= 0; --u)
+        if (unpack_max<T>(h[u]) == gm) gv = v + 32 * u;
     }
-    if (a4[2] > m0) {
-      m0 = a4[2];
-      i0 = v + 64;
-    }
-    if (a4[3] > m1) {
-      m1 = a4[3];
-      i1 = v + 96;
-    }
+  };
+  int v = vb + lane;
+#pragma unroll 2
+  for (; v + 96 < ve; v += 128) {
+    uint4 x[4];
+    load_group<T, false>(sv, v, ve, x);
+    group(x, v);
+  }
+  if (v < ve) {
+    uint4 x[4];
+    load_group<T, true>(sv, v, ve, x);
+    group(x, v);
   }
   if (nanacc != nanacc || nanacc == INFINITY) a.bad = 1;
-  if (m1 > m0 || (m1 == m0 && i1 < i0)) {
-    m0 = m1;
-    i0 = i1;
-  }
-  if (m0 > a.m) {
-    const uint4 x = sv[i0];
-    int e = 0;
-#pragma unroll
-    for (int t = kVec - 1; t >= 0; --t)
-      if (vec_elem<T>(x, t) == m0) e = t;
-    acc_raise<SAMPLED>(a, m0, ebase + i0 * kVec + e, c);
-  }
+  if (M == -INFINITY) return;
   if (SAMPLED) {
-    const float mm = (a.m == -INFINITY) ? 0.f : scaled_ref(a.m, c);
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    for (int w = vb + lane; w < ve; w += 128) {
-      s0 += vec_exp_sum<T>(vec_or_neg_inf<T>(sv, w, ve), mm, c);
-      s1 += vec_exp_sum<T>(vec_or_neg_inf<T>(sv, w + 32, ve), mm, c);
-      s2 += vec_exp_sum<T>(vec_or_neg_inf<T>(sv, w + 64, ve), mm, c);
-      s3 += vec_exp_sum<T>(vec_or_neg_inf<T>(sv, w + 96, ve), mm, c);
-    }
-    a.s += (s0 + s1) + (s2 + s3);
+    const int e = (M >= a.m) ? ebase + vec_find<T>(sv, gv, M) : INT_MAX;  // index only matters then
+    merge_part<true>(a.m, a.s, a.idx, M, S, e, c);
+  } else if (M > a.m) {
+    acc_raise<false>(a, M, ebase + vec_find<T>(sv, gv, M), c);
   }
 }
 
@@ -757,21 +767,25 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   } else {
     // Consumer warps.  The work items are (chunk, piece): chunk ch of the ring
     // sequence is split into kPieces ranges of vectors, and warp w takes items
-    // w, w + 8, ...  Warps therefore work on different chunks at once and only
-    // meet at the end.  A warp merges its lanes only when its row changes.
+    // w, w + kConsumerWarps, ...  Warps therefore work on different chunks at
+    // once and only meet at the end.  A warp merges its lanes only when its
+    // row changes.
     if (sampled)
       for (int s = 0; s < nstreams; ++s)
         if (lane == 0) sh.wpart[s][warp] = identity_partial();
     bool ok = true;
     if (ALIGNED && body > 0) {
       const int nch = (body + slot_elems - 1) / slot_elems;  // chunks per row
-      const int items = nstreams * nch * kPieces;
       int cur = -1;
       Acc a;
       acc_init(a);
-      for (int i = warp; i < items && ok; i += kConsumerWarps) {
-        const int ch = i / kPieces, q = i % kPieces;
-        const int s = ch / nch, ci = ch % nch;
+      // Item (chunk ch, piece q) of warp w: q = w mod kPieces, ch = w / kPieces,
+      // then every kGroups-th chunk; row s and chunk-in-row ci, ring slot and
+      // phase parity advance with it.
+      const int q = warp % kPieces;
+      int s = (warp / kPieces) / nch, ci = (warp / kPieces) % nch;
+      uint32_t slot = static_cast<uint32_t>(warp / kPieces), par = 0;  // first chunk < kGroups <= nslots
+      for (; s < nstreams && ok;) {
         if (s != cur) {
           if (cur >= 0) {
             if (sampled) {
@@ -784,8 +798,6 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
           acc_init(a);
           cur = s;
         }
-        const uint32_t slot = static_cast<uint32_t>(ch) % nslots;
-        const uint32_t par = (static_cast<uint32_t>(ch) / nslots) & 1u;
         if (!mbar_wait_bounded(&sh.full[slot], par)) {
           ok = false;
           break;
@@ -799,6 +811,16 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
         else acc_range<T, false>(a, sv, vb, ve, v0 + c0, c, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.empty[slot]);
+        ci += kGroups;
+        while (ci >= nch) {
+          ci -= nch;
+          ++s;
+        }
+        slot += kGroups;
+        if (slot >= static_cast<uint32_t>(nslots)) {
+          slot -= nslots;
+          par ^= 1u;
+        }
       }
       if (cur >= 0) {
         const uint32_t fl = acc_bad(a) | (ok ? 0u : kTimedOut);
