@@ -232,14 +232,14 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 
 namespace specv {
 
-// log2(x) for finite x > 0 as exponent + log2(mantissa in [1, 2)): the fp32
-// log2 of the mantissa is accurate to about 1e-7 absolute, so the result keeps
-// that absolute accuracy however large the exponent.  log2(0) = -inf.
-__device__ __forceinline__ double log2_split(float x) {
-  if (x == 0.f) return -INFINITY;
+// log2(x) for a normal x > 0 split into an exact integer part and a
+// fraction in [0, 1): x = m * 2^e with m in [1, 2); the fraction is log2f(m),
+// accurate to about one unit of 2^-24.
+__device__ __forceinline__ void log2_parts(float x, float& ip, float& fp) {
   int e;
   const float m = frexpf(x, &e);  // x = m * 2^e, m in [0.5, 1)
-  return static_cast<double>(e - 1) + static_cast<double>(log2f(2.f * m));
+  ip = static_cast<float>(e - 1);
+  fp = log2f(2.f * m);
 }
 
 }  // namespace specv

@@ -6,12 +6,15 @@
 // (ignis docs, "Speculative decoding" -- "One round, step by step", steps 3-4).
 //
 //   pass 1   a producer thread streams the slices through a shared-memory ring
-//            with bulk (TMA) copies; eight consumer warps keep, per thread, the
-//            running argmax (lowest index on ties) and, for sampled lanes, the
-//            online max / sum of 2^((x - max) * log2(e) / T)
-//   reduce   warp shuffles -> per-CTA partial per row -> pushed into every CTA
-//            of the cluster through distributed shared memory
-//   scan     every CTA finishes the per-row reductions and runs the lane's
+//            with bulk (TMA) copies; sixteen consumer warps take (chunk, piece)
+//            items and keep, per lane, the running max, the first vector
+//            holding it and, for sampled lanes, the sum of
+//            2^(x * log2(e) / T - fl(max * log2(e) / T))
+//   reduce   greedy rows: one 64-bit key (ordered max, complemented index) per
+//            row, combined with shared-memory atomics and sent to the leader
+//            CTA; sampled rows: per-warp partials merged per CTA and pushed
+//            into every CTA of the cluster through distributed shared memory
+//   scan     the leader (greedy) or every CTA (sampled) runs the lane's
 //            acceptance scan (<= 15 drafts, one lane of warp 0 per position)
 //   pass 2   sampled lanes only: the cluster re-reads one target row (and one
 //            drafter row) from L2, sums the draw weights per slice, exchanges the
@@ -19,7 +22,8 @@
 //
 // Greedy lanes compare raw logits only, so their results are exact.  Sampled
 // lanes use fp32 with the hardware exp2; the acceptance test is done in the
-// log2 domain: accept iff log2(u) < log2 p(d) - log2 q(d).
+// log2 domain, accept iff log2(u) < log2 p(d) - log2 q(d), as a compensated
+// fp32 sum of exactly represented terms.
 #pragma once
 
 #include <cfloat>
@@ -50,6 +54,10 @@ constexpr int kDrawRound = 256;  // elements per warp per pass-2 round (32 lanes
 #define SPEC_VERIFY_PIECES 4
 #endif
 constexpr int kPieces = SPEC_VERIFY_PIECES;  // warps sharing one chunk of the ring
+#ifndef SPEC_VERIFY_UNROLL
+#define SPEC_VERIFY_UNROLL 2
+#endif
+constexpr int kGroupUnroll = SPEC_VERIFY_UNROLL;  // groups per iteration of the sweep loop
 // Consumer warps form kGroups groups of kPieces; group g takes the chunks
 // ch = g (mod kGroups).  The ring must have a multiple of kGroups slots so
 // that every slot belongs to one group: a warp then only ever waits on a slot
@@ -59,7 +67,7 @@ constexpr int kGroups = kConsumerWarps / kPieces;
 static_assert(kConsumerWarps % kPieces == 0, "consumer warps must form whole groups");
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr double kLn2d = 0.6931471805599453;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // Partial reduction of one row over some elements (16 bytes, pushed over DSMEM).
 struct __align__(16) Partial {
@@ -387,7 +395,7 @@ __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int v
     }
   };
   int v = vb + lane;
-#pragma unroll 2
+#pragma unroll kGroupUnroll
   for (; v + 96 < ve; v += 128) {
     uint4 x[4];
     load_group<T, false>(sv, v, ve, x);
@@ -465,6 +473,48 @@ __device__ __forceinline__ void fold_greedy_row(SmemHead& sh, int s, float m, in
   const int I = __reduce_min_sync(0xFFFFFFFFu, (m == M) ? idx : INT_MAX);
   if (flags) atomicOr(&sh.cta_flags, flags);
   if (lane == 0 && I != INT_MAX) atomicMax(&sh.gkey[s], argmax_key(M, I));
+}
+
+// ---------------------------------------------------------------------------
+// Compensated fp32 sums for the acceptance test
+// ---------------------------------------------------------------------------
+// a + b = s + e exactly (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float z = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
+}
+
+// Running sum with the rounding errors of every addition carried alongside
+// (Ogita, Rump and Oishi, "Accurate sum and dot product", Algorithm Sum2):
+// the result is as accurate as a sum in twice the working precision, then
+// rounded once.
+struct CompSum {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    float t, e;
+    two_sum(s, x, t, e);
+    s = t;
+    c = __fadd_rn(c, e);
+  }
+  __device__ __forceinline__ float value() const { return __fadd_rn(s, c); }
+};
+
+// log2 p(d) of a row in the terms its sum was taken in,
+//   x_d * c - fl(max * c) - log2(S),
+// as a compensated sum: x_d * c split exactly into fl(x_d * c) and the FMA
+// remainder, log2(S) into its exact exponent and its fraction.
+__device__ __forceinline__ CompSum log2_prob_terms(float xd, const Partial& row, float c) {
+  float ip, fp;
+  log2_parts(row.s, ip, fp);
+  const float t = __fmul_rn(xd, c);
+  CompSum r;
+  r.add(t);
+  r.add(-scaled_ref(row.m, c));
+  r.add(-ip);
+  r.add(-fp);
+  r.add(__fmaf_rn(xd, c, -t));
+  return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -943,23 +993,33 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     }
 
     int n = 0, mode = kNoDraw;
-    // log2 p_j(d) and log2 q_j(d) at this lane's position, in the terms the
-    // sums were taken in:  x_d * c - fl(max * c) - log2(S).  x_d * c is exact
-    // in fp64 and log2(S) is accurate to ~1e-7, so both carry ~1e-7 error.
-    double lp = NAN, lq = NAN;
+    // log2 p_j(d) and log2 q_j(d) at this lane's position, and the test
+    // log2(u) < log2 p - log2 q, as one compensated fp32 sum of exact terms:
+    // its rounding error is far below the ~1e-6 relative error of the sums S.
+    float lp = NAN, lq = NAN;
     if (st == SPEC_OK) {
       const bool active = lane < k;
       bool accept = true;
       if (active) {
-        const double cd = static_cast<double>(c);
-        const Partial pt = sh.fin[2 * lane], pq = sh.fin[2 * lane + 1];
-        lp = (static_cast<double>(sh.xd_t[lane]) * cd - static_cast<double>(scaled_ref(pt.m, c))) -
-             log2_split(pt.s);
-        lq = (static_cast<double>(sh.xd_q[lane]) * cd - static_cast<double>(scaled_ref(pq.m, c))) -
-             log2_split(pq.s);
-        if (lp == -INFINITY) accept = false;
-        else if (lq == -INFINITY) accept = true;
-        else accept = log2_split(sh.u_acc[lane]) < lp - lq;
+        const float xt = sh.xd_t[lane], xq = sh.xd_q[lane];
+        CompSum dp = log2_prob_terms(xt, sh.fin[2 * lane], c);
+        const CompSum dq = log2_prob_terms(xq, sh.fin[2 * lane + 1], c);
+        lp = (xt == -INFINITY) ? -INFINITY : dp.value();
+        lq = (xq == -INFINITY) ? -INFINITY : dq.value();
+        const float u = sh.u_acc[lane];
+        if (xt == -INFINITY) {
+          accept = false;  // p(d) = 0
+        } else if (xq == -INFINITY || u == 0.f) {
+          accept = true;   // q(d) = 0, or log2(u) = -inf
+        } else {
+          float iu, fu;
+          log2_parts(u, iu, fu);
+          dp.add(-dq.s);
+          dp.add(-dq.c);
+          dp.add(-iu);
+          dp.add(-fu);
+          accept = dp.value() > 0.f;
+        }
       }
       const uint32_t mask = __ballot_sync(0xFFFFFFFFu, active && !accept);
       n = mask ? (__ffs(mask) - 1) : k;
@@ -986,9 +1046,15 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
           const Partial pt = sh.fin[2 * j];
           rs->argmax = pt.idx;
           rs->max_logit = pt.m;
-          rs->lse = static_cast<float>((static_cast<double>(scaled_ref(pt.m, c)) + log2_split(pt.s)) * kLn2d);
-          rs->logp_d = (j < k) ? static_cast<float>(lp * kLn2d) : NAN;
-          rs->logq_d = (j < k) ? static_cast<float>(lq * kLn2d) : NAN;
+          float ip, fp;
+          log2_parts(pt.s, ip, fp);
+          CompSum l;
+          l.add(scaled_ref(pt.m, c));
+          l.add(ip);
+          l.add(fp);
+          rs->lse = __fmul_rn(l.value(), kLn2);
+          rs->logp_d = (j < k) ? __fmul_rn(lp, kLn2) : NAN;
+          rs->logq_d = (j < k) ? __fmul_rn(lq, kLn2) : NAN;
           if (!(drawn_here && mode == kResidual)) rs->resid_mass = NAN;
           if (!drawn_here) rs->drawn = -1;
           rs->flags = 1 | (drawn_here ? (mode == kResidual ? 2 : 4) : 0);
@@ -1007,7 +1073,13 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   int draw_row = residual ? n : k;  // target row whose p enters the weights
   const uint8_t* qrow = p.draft + static_cast<int64_t>(off + n) * p.ld_bytes;
   const float uprime = sh.u_smp[n];
-  const int seg = ((span + kConsumerWarps - 1) / kConsumerWarps + kDrawRound - 1) / kDrawRound * kDrawRound;
+  // Each consumer warp walks one segment of the slice (a multiple of 8
+  // elements, so rounds start 16-byte aligned; the last round may be partial).
+#ifndef SPEC_VERIFY_SEG_ROUND
+#define SPEC_VERIFY_SEG_ROUND 256
+#endif
+  const int seg = ((span + kConsumerWarps - 1) / kConsumerWarps + SPEC_VERIFY_SEG_ROUND - 1) /
+                  SPEC_VERIFY_SEG_ROUND * SPEC_VERIFY_SEG_ROUND;
   auto make_coef = [&]() {
     DrawCoef kc;
     const Partial pt = sh.fin[2 * draw_row];
@@ -1155,49 +1227,49 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
         }
 #pragma unroll
         for (int u = 0; u < kDrawBatch; ++u) {
-        const int base = bbase + u * kDrawRound;
-        if (base >= s1 || found >= 0) break;
-        float w[8], cum[8];
-        const int e = base + lane * 8;
-        draw_piece<T>(kc, rt[u], rq[u], e, s1, w, cum);
-        const float R = warp_sum_xor(cum[7]);
-        const float next = __fadd_rn(run, R);
-        if (next > tau1) {
-          // The crossing is in this round: inclusive scan over the lanes.
-          const float tau2 = __fsub_rn(tau1, run);
-          float incl = cum[7];
+          const int base = bbase + u * kDrawRound;
+          if (base >= s1 || found >= 0) break;
+          float w[8], cum[8];
+          const int e = base + lane * 8;
+          draw_piece<T>(kc, rt[u], rq[u], e, s1, w, cum);
+          const float R = warp_sum_xor(cum[7]);
+          const float next = __fadd_rn(run, R);
+          if (next > tau1) {
+            // The crossing is in this round: inclusive scan over the lanes.
+            const float tau2 = __fsub_rn(tau1, run);
+            float incl = cum[7];
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float up = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl = __fadd_rn(up, incl);
-          }
-          float excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-          if (lane == 0) excl = 0.f;
-          const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl > tau2);
-          int tok = -1;
-          if (hit) {
-            const int l = __ffs(hit) - 1;
-            if (lane == l) {
-              const float tau3 = __fsub_rn(tau2, excl);
-              int t = -1, lastpos = -1;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                if (w[i] > 0.f) lastpos = e + i;
-                if (t < 0 && cum[i] > tau3) t = e + i;
-              }
-              tok = (t >= 0) ? t : lastpos;
+            for (int o = 1; o < 32; o <<= 1) {
+              const float up = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+              if (lane >= o) incl = __fadd_rn(up, incl);
             }
-            tok = __shfl_sync(0xFFFFFFFFu, tok, l);
-          } else {
-            int lastpos = -1;
+            float excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+            if (lane == 0) excl = 0.f;
+            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl > tau2);
+            int tok = -1;
+            if (hit) {
+              const int l = __ffs(hit) - 1;
+              if (lane == l) {
+                const float tau3 = __fsub_rn(tau2, excl);
+                int t = -1, lastpos = -1;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (w[i] > 0.f) lastpos = e + i;
-            tok = warp_max_int(lastpos);
+                for (int i = 0; i < 8; ++i) {
+                  if (w[i] > 0.f) lastpos = e + i;
+                  if (t < 0 && cum[i] > tau3) t = e + i;
+                }
+                tok = (t >= 0) ? t : lastpos;
+              }
+              tok = __shfl_sync(0xFFFFFFFFu, tok, l);
+            } else {
+              int lastpos = -1;
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (w[i] > 0.f) lastpos = e + i;
+              tok = warp_max_int(lastpos);
+            }
+            found = tok;
           }
-          found = tok;
-        }
-        run = next;
+          run = next;
         }
       }
       if (found < 0) found = sh.seglast[warp];
