@@ -61,6 +61,7 @@ struct VerifyShape {
   int nslots;
   int head_bytes;
   int smem;
+  int active;  // clusters of this shape resident at once (0 if unknown)
 };
 
 // One cluster of `cluster` CTAs per lane; each CTA reduces `slice` elements of
@@ -213,6 +214,7 @@ int resolve_shape(DeviceCache* dc, int dev, int lanes, int rows, int V, int dtyp
   const bool forced = env_int("SPEC_VERIFY_CLUSTER", 0) > 0;
   for (;;) {
     const int active = max_active_clusters(dev, kernel, s.cluster, s.smem);
+    s.active = active;
     const bool few = static_cast<int64_t>(lanes) * s.cluster <= 2LL * dc->sms;
     if (s.cluster == 1 || (active > 0 && (forced || !few || active >= lanes))) break;
     s = choose_shape(lanes, rows, V, esize, aligned, dc->sms, dc->smem_optin, smaller_cluster(s.cluster));
@@ -325,6 +327,9 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
   p.slot_bytes = s.slot_bytes;
   p.nslots = s.nslots;
   p.head_bytes = s.head_bytes;
+  // More lanes than resident clusters: take them longest first.
+  const int order_env = env_int("SPEC_VERIFY_ORDER", -1);
+  p.order_by_cost = order_env >= 0 ? (order_env != 0) : (s.active > 0 && a->lanes > s.active);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(s.cluster * a->lanes), 1, 1);

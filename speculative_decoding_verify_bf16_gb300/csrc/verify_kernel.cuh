@@ -47,6 +47,8 @@ constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps;    // streams the slices (lane 0)
 constexpr int kHelperWarp = kConsumerWarps + 1;  // draft tokens, logits at them, uniforms
 constexpr int kThreads = kConsumers + 64;
+constexpr int kWarps = kThreads / 32;
+constexpr int kCostBuckets = 64;  // lane cost classes for the longest-first lane order
 constexpr int kMaxCluster = 16;
 constexpr int kMaxSlots = 32;
 constexpr int kDrawRound = 256;  // elements per warp per pass-2 round (32 lanes x 8)
@@ -108,6 +110,9 @@ struct __align__(16) SmemHead {
   int scan_n;
   int scan_mode;
   uint32_t cta_flags;
+  int order_hist[kCostBuckets];  // lanes per cost class (longest-first lane order)
+  int order_cnt[kWarps];
+  int order_bucket, order_j, order_w, order_j2, order_lane;
 };
 
 struct VerifyParams {
@@ -132,6 +137,7 @@ struct VerifyParams {
   int32_t slot_bytes;  // bytes per ring slot (multiple of 16)
   int32_t nslots;
   int32_t head_bytes;  // offset of the ring in dynamic shared memory
+  int32_t order_by_cost;  // clusters take lanes in order of decreasing cost (more lanes than fit at once)
 };
 
 // ---------------------------------------------------------------------------
@@ -681,6 +687,93 @@ __device__ __forceinline__ void greedy_finish(const VerifyParams& p, const SmemH
   }
 }
 
+// Estimated cost class of lane b: the rows it streams, a sampled row pair
+// (target and drafter, with exponentials) counting twice a greedy row, plus
+// one for the draw.  Lanes that will fail their checks cost 0.
+__device__ __forceinline__ int lane_cost(const VerifyParams& p, int b) {
+  const int k = __ldg(p.draft_lens + b);
+  const float t = __ldg(p.temps + b);
+  if (k < 0 || k > kMaxDrafts) return 0;
+  return (t > 0.f) ? 4 * k + 3 : k + 1;  // < kCostBuckets
+}
+
+// The lane of rank `rank` when lanes are sorted by decreasing cost class
+// (ties by index).  Clusters start roughly in index order, so when there are
+// more lanes than resident clusters, mapping cluster i to the lane of rank i
+// starts the costliest lanes first and lets cheap ones fill the last waves
+// (longest-processing-time-first list scheduling).  Every CTA computes the
+// same permutation from the lane metadata: a histogram of the cost classes,
+// the class holding the rank, then that class's members counted in index
+// order.  Called by all threads; returns the same lane in every thread.
+__device__ int lane_of_rank(const VerifyParams& p, SmemHead& sh, int rank) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid < kCostBuckets) sh.order_hist[tid] = 0;
+  __syncthreads();
+  for (int b = tid; b < p.lanes; b += kThreads) atomicAdd(&sh.order_hist[lane_cost(p, b)], 1);
+  __syncthreads();
+  if (warp == 0) {
+    // Lane l holds classes 63 - 2l and 62 - 2l; higher classes rank first.
+    const int c0 = kCostBuckets - 1 - 2 * lane, c1 = c0 - 1;
+    const int h0 = sh.order_hist[c0], h1 = sh.order_hist[c1];
+    int incl = h0 + h1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int up = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += up;
+    }
+    const int excl = incl - h0 - h1;
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, incl > rank);
+    if (lane == __ffs(m) - 1) {
+      const bool first = rank < excl + h0;
+      sh.order_bucket = first ? c0 : c1;
+      sh.order_j = first ? rank - excl : rank - excl - h0;
+    }
+  }
+  __syncthreads();
+  const int c = sh.order_bucket, j = sh.order_j;
+  const int per = (p.lanes + kWarps - 1) / kWarps;
+  const int lo = min(p.lanes, warp * per), hi = min(p.lanes, lo + per);
+  int cnt = 0;
+  for (int b = lo + lane; b < hi; b += 32) cnt += (lane_cost(p, b) == c) ? 1 : 0;
+  cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+  if (lane == 0) sh.order_cnt[warp] = cnt;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = (lane < kWarps) ? sh.order_cnt[lane] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int up = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += up;
+    }
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, incl > j);
+    if (lane == __ffs(m) - 1) {
+      sh.order_w = lane;
+      sh.order_j2 = j - (incl - v);
+    }
+  }
+  __syncthreads();
+  if (warp == sh.order_w) {
+    int need = sh.order_j2;
+    for (int base = lo; base < hi; base += 32) {
+      const int b = base + lane;
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, b < hi && lane_cost(p, b) == c);
+      const int n = __popc(m);
+      if (need < n) {
+        if (lane == 0) {
+          uint32_t mm = m;
+          for (int t = 0; t < need; ++t) mm &= mm - 1;  // drop the `need` lowest set bits
+          sh.order_lane = base + __ffs(mm) - 1;
+        }
+        break;
+      }
+      need -= n;
+    }
+  }
+  __syncthreads();
+  return sh.order_lane;
+}
+
 template <typename T, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_accept_kernel(const VerifyParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -696,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   const int C = p.cluster;
   const uint32_t rank = cluster_ctarank();
   const bool leader = (rank == 0);
-  const int b = blockIdx.x / C;
+  int b = blockIdx.x / C;
 
   // ---- set-up that touches only shared memory (overlaps the previous kernel) ----
   if (tid == 0) {
@@ -712,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   }
   if (tid <= kMaxDrafts) sh.gkey[tid] = 0ull;
   griddep_wait();
+  if (p.order_by_cost) b = lane_of_rank(p, sh, b);
 
   // ---- lane metadata (read by every thread; one transaction per warp) ----
   const int k = __ldg(p.draft_lens + b);

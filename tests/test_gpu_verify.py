@@ -273,6 +273,24 @@ def test_results_do_not_depend_on_the_cluster_shape(monkeypatch):
             assert (g["committed"][greedy] == ref["committed"][greedy]).all()
 
 
+@pytest.mark.parametrize("lanes,vocab,kmax", [(300, 3000, 7), (9, 40000, 7), (200, 20000, 3)])
+def test_longest_first_lane_order_changes_nothing(monkeypatch, lanes, vocab, kmax):
+    """With more lanes than resident clusters the kernel maps clusters to lanes
+    in order of decreasing cost (300 lanes of V=3000 do so by themselves);
+    forcing that order on or off must give bit-identical outputs, equal to the
+    oracle's."""
+    r = workloads.make_custom_round(41 + lanes, DEV, lanes=lanes, vocab=vocab, kmax=kmax, dtype="bf16",
+                                    sampled="mixed")
+    orc = run_oracle(r)
+    runs = {}
+    for order in ("0", "1"):
+        monkeypatch.setenv("SPEC_VERIFY_ORDER", order)
+        runs[order] = run_gpu(r)
+        compare(r, runs[order], orc)
+    for key in ("committed", "out_tokens", "lane_status"):
+        np.testing.assert_array_equal(runs["0"][key], runs["1"][key], err_msg=key)
+
+
 @pytest.mark.parametrize("cluster,ring_kb,slot_kb", [("4", "75", "32"), ("12", "75", "32"), ("16", "88", "32"),
                                                       ("8", "40", "8"), ("2", "100", "32")])
 def test_back_to_back_graph_launches_are_identical(monkeypatch, cluster, ring_kb, slot_kb):
