@@ -408,6 +408,167 @@ def check_commit_copies_column_committed_minus_one():
     assert st.tolist() == [0, 0, 0, oracle.STATUS_LAYOUT, oracle.STATUS_NONFINITE]
 
 
+# ---------------------------------------------------------------------------
+# Acceptance metrics: strata2signal "Acceptance: three numbers with one name"
+# ---------------------------------------------------------------------------
+import os
+
+from oracle import backoff as ob
+from oracle import metrics as om
+
+_GOLDEN_DIR = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rates():
+    out = {}
+    with open(os.path.join(_GOLDEN_DIR, "acceptance_rates_worked_example.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                name, value, decimals = line.split()
+                out[name] = (float(value), int(decimals))
+    return out
+
+
+def _printed(value, printed):
+    """value, rounded as the page rounds it, equals the printed figure."""
+    want, decimals = printed
+    assert abs(value - want) <= 0.5 * 10.0 ** (-decimals) + 1e-12, (value, want)
+
+
+def check_acceptance_metrics_worked_example():
+    """The page's 43 rounds give every figure its table prints."""
+    counts = om.AcceptCounts()
+    for k, n, times in read_golden("acceptance_rounds_worked_example.txt"):
+        for _ in range(times):
+            om.count_round(counts, k, n)
+    assert (counts.rounds, counts.proposed, counts.accepted) == (43, 171, 84)
+    assert counts.slot_kept[:4] == [37, 24, 16, 7]
+    g = _golden_rates()
+    r = om.accept_rates(counts)
+    _printed(r.accepted_per_proposed, g["accepted_per_proposed"])
+    _printed(r.tokens_per_round, g["tokens_per_round"])
+    for j in range(4):
+        _printed(r.by_slot[j], g[f"by_slot_{j + 1}"])
+        _printed(r.given_previous[j], g[f"given_previous_{j + 1}"])
+    assert r.depth == 4
+    _printed(r.implied_alpha, g["implied_alpha"])
+    # "one plus their sum is 2.95 again"
+    _printed(1.0 + sum(r.by_slot), g["tokens_per_round"])
+    llama = om.AcceptCounts(rounds=1, proposed=297, accepted=171)
+    _printed(om.accept_rates(llama).accepted_per_proposed, g["llama_accepted_per_proposed"])
+
+
+def check_acceptance_metrics_identities(seed=5):
+    """On random rounds: one plus the by-slot shares is the tokens a round;
+    the given-previous shares multiply up to the by-slot shares; the implied
+    alpha reproduces the tokens a round; rounds that proposed nothing still
+    count as rounds."""
+    rng = np.random.default_rng(seed)
+    for trial in range(20):
+        counts = om.AcceptCounts()
+        for _ in range(int(rng.integers(1, 200))):
+            k = int(rng.integers(0, 16))
+            om.count_round(counts, k, int(rng.integers(0, k + 1)))
+        r = om.accept_rates(counts)
+        assert abs(1.0 + sum(r.by_slot) - r.tokens_per_round) < 1e-12
+        prod = 1.0
+        for j in range(om.MAX_SLOTS):
+            if counts.slot_kept[j] == 0:
+                break
+            prod *= r.given_previous[j]
+            assert abs(prod - r.by_slot[j]) < 1e-12
+        assert sum(counts.slot_kept) == counts.accepted
+        assert sum(counts.slot_reached) == counts.proposed
+        if r.depth > 0 and 1.0 < r.tokens_per_round < r.depth + 1.0:
+            assert abs(om.tokens_a_round_of_alpha(r.implied_alpha, r.depth) - r.tokens_per_round) < 1e-9
+
+
+def check_implied_alpha_recovers_independent_guesses(seed=11, rounds=200000):
+    """Guesses that each survive with probability alpha, independently, give an
+    implied alpha close to alpha (the textbook model the page's alpha assumes)."""
+    rng = np.random.default_rng(seed)
+    for alpha, depth in ((0.73, 4), (0.5, 7), (0.9, 3)):
+        survive = rng.random((rounds, depth)) < alpha
+        kept = np.argmin(np.concatenate([survive, np.zeros((rounds, 1), bool)], axis=1), axis=1)
+        counts = om.AcceptCounts()
+        counts.rounds, counts.proposed, counts.accepted = rounds, rounds * depth, int(kept.sum())
+        r = om.accept_rates(counts)
+        assert abs(r.implied_alpha - alpha) < 0.01, (alpha, r.implied_alpha)
+
+
+def check_metrics_from_verify_outputs():
+    """Counting a verify round's outputs: a lane proposes draft_lens[b] and keeps
+    committed[b] - 1; failed lanes are left out."""
+    counts = om.count_verify_outputs(om.AcceptCounts(), committed=[1, 4, 3, 0, 2], draft_lens=[3, 3, 7, 2, 1],
+                                     lane_status=[0, 0, 0, oracle.STATUS_LAYOUT, 0])
+    assert (counts.rounds, counts.proposed, counts.accepted) == (4, 14, 6)
+    assert counts.slot_kept[:4] == [3, 2, 1, 0]
+    assert counts.slot_reached[:8] == [4, 3, 3, 1, 1, 1, 1, 0]
+
+
+# ---------------------------------------------------------------------------
+# Miss back-off: mashbox "Speculative decoding", "What it does for you"
+# ---------------------------------------------------------------------------
+def _guess_pattern(n_passes, kept_when_guessing, lanes=1, others_guess=True):
+    """Run lane 0 through n_passes; it keeps kept_when_guessing(i) guesses in
+    pass i when it may guess (3 proposed).  Returns the string of passes:
+    'g' guessed, 'w' waited."""
+    states = [ob.BackoffState() for _ in range(lanes)]
+    out = []
+    for i in range(n_passes):
+        prop = [3 if ob.may_guess(s) else 0 for s in states]
+        kept = [0] * lanes
+        if prop[0]:
+            kept[0] = kept_when_guessing(i)
+        if not others_guess:
+            for b in range(1, lanes):
+                prop[b] = 0
+        out.append("g" if prop[0] else "w")
+        ob.step(states, prop, kept)
+    return "".join(out)
+
+
+def check_backoff_waits_16_then_doubles_to_256():
+    """Misses only: 4 passes guess, then 16 wait; each further 4 misses double
+    the wait, up to 256."""
+    want = ""
+    for w in (16, 32, 64, 128, 256, 256):
+        want += "gggg" + "w" * w
+    want += "gggg"
+    pat = _guess_pattern(len(want), lambda i: 0)
+    assert pat == want, pat
+
+
+def check_backoff_kept_guess_resets():
+    """A pass that keeps a guess ends the miss run and sets the wait back to 16."""
+    # 3 misses, a keep, then misses: the first wait starts after 4 more misses
+    pat = _guess_pattern(3 + 1 + 4 + 16 + 1, lambda i: 1 if i == 3 else 0)
+    assert pat == "ggg" + "g" + "gggg" + "w" * 16 + "g", pat
+    # the wait doubles to 32, then a keep after it brings the next wait back to 16
+    seq = "gggg" + "w" * 16 + "gggg" + "w" * 32
+    keep_at = len(seq)  # first pass after the 32-pass wait keeps a guess
+    pat = _guess_pattern(len(seq) + 1 + 4 + 16 + 1, lambda i: 1 if i == keep_at else 0)
+    assert pat == seq + "g" + "gggg" + "w" * 16 + "g", pat
+
+
+def check_backoff_passes_without_speculation():
+    """A pass in which no lane of the batch has a guess counts toward no miss
+    run (and does not break one), only toward a wait already running; a lane
+    that may guess but has no guess in a pass that speculates counts a miss."""
+    s = [ob.BackoffState(), ob.BackoffState()]
+    for _ in range(3):  # lane 0 misses 3 times, lane 1 guesses and keeps
+        ob.step(s, [2, 2], [0, 1])
+    ob.step(s, [0, 0], [0, 0])  # nobody guesses: not counted
+    assert s[0].misses == 3 and s[0].wait == 0
+    ob.step(s, [0, 2], [0, 1])  # lane 0 has no guess in a pass that speculates: a miss
+    assert s[0].wait == 16 and s[0].misses == 0 and s[0].backoff == 32
+    for _ in range(5):  # waiting counts down in passes that do not speculate too
+        ob.step(s, [0, 0], [0, 0])
+    assert s[0].wait == 11
+    assert ob.next_draft_lens(s, 5) == [0, 5]
+
+
 ALL_CHECKS = [
     check_row_budget_worked_example,
     check_guess_check_table,
@@ -421,4 +582,11 @@ ALL_CHECKS = [
     check_softmax_against_scipy,
     check_decode_bf16_against_torch,
     check_commit_copies_column_committed_minus_one,
+    check_acceptance_metrics_worked_example,
+    check_acceptance_metrics_identities,
+    check_implied_alpha_recovers_independent_guesses,
+    check_metrics_from_verify_outputs,
+    check_backoff_waits_16_then_doubles_to_256,
+    check_backoff_kept_guess_resets,
+    check_backoff_passes_without_speculation,
 ]

@@ -67,6 +67,37 @@ def _commit_wrong_column(staged, live, committed, lane_status=None):
     return out
 
 
+import oracle.backoff as ob
+import oracle.metrics as om
+
+
+def _rates_by_slot_over_proposed(counts):
+    r = _orig_accept_rates(counts)
+    r.by_slot = [counts.slot_kept[j] / counts.slot_reached[j] if counts.slot_reached[j] else float("nan")
+                 for j in range(om.MAX_SLOTS)]
+    return r
+
+
+def _rates_given_over_rounds(counts):
+    r = _orig_accept_rates(counts)
+    r.given_previous = [counts.slot_kept[j] / counts.rounds for j in range(om.MAX_SLOTS)]
+    return r
+
+
+def _rates_tokens_without_own(counts):
+    r = _orig_accept_rates(counts)
+    r.tokens_per_round = counts.accepted / counts.rounds
+    return r
+
+
+def _alpha_depth_off_by_one(tokens_a_round, depth, iters=200):
+    return _orig_implied_alpha(tokens_a_round, depth + 1, iters)
+
+
+_orig_accept_rates = om.accept_rates
+_orig_implied_alpha = om.implied_alpha
+
+
 MUTATIONS = [
     ("argmax ties to the highest index", ov, "argmax_lowest", _argmax_last,
      oc.check_greedy_equals_plain_decode),
@@ -86,6 +117,17 @@ MUTATIONS = [
      oc.check_row_budget_worked_example),
     ("commit copies column c", oracle, "commit_state", _commit_wrong_column,
      oc.check_commit_copies_column_committed_minus_one),
+    ("by-slot share over rounds that proposed the slot", om, "accept_rates", _rates_by_slot_over_proposed,
+     oc.check_acceptance_metrics_worked_example),
+    ("given-previous share over all rounds", om, "accept_rates", _rates_given_over_rounds,
+     oc.check_acceptance_metrics_worked_example),
+    ("tokens a round without the model's own token", om, "accept_rates", _rates_tokens_without_own,
+     oc.check_acceptance_metrics_worked_example),
+    ("implied alpha at depth + 1", om, "implied_alpha", _alpha_depth_off_by_one,
+     oc.check_acceptance_metrics_worked_example),
+    ("back-off after 3 misses", ob, "MISSES_TO_WAIT", 3, oc.check_backoff_waits_16_then_doubles_to_256),
+    ("back-off capped at 128", ob, "LONGEST_WAIT", 128, oc.check_backoff_waits_16_then_doubles_to_256),
+    ("first wait 8 passes", ob, "FIRST_WAIT", 8, oc.check_backoff_kept_guess_resets),
 ]
 
 
@@ -100,6 +142,45 @@ def test_commit_mistake_breaks_no_trace(monkeypatch):
     monkeypatch.setattr(oracle, "commit_state", _commit_wrong_column)
     with pytest.raises(AssertionError):
         oc.check_greedy_equals_plain_decode()
+
+
+def _step_counts_every_pass(states, proposed, kept):
+    for b, st in enumerate(states):
+        if st.wait > 0:
+            st.wait -= 1
+            continue
+        if kept[b] > 0:
+            st.misses, st.backoff = 0, ob.FIRST_WAIT
+            continue
+        st.misses += 1
+        if st.misses == ob.MISSES_TO_WAIT:
+            st.wait, st.backoff, st.misses = st.backoff, min(2 * st.backoff, ob.LONGEST_WAIT), 0
+    return [ob.may_guess(st) for st in states]
+
+
+def _step_keep_during_run_not_reset(states, proposed, kept):
+    speculates = any(p > 0 for p in proposed)
+    for b, st in enumerate(states):
+        if st.wait > 0:
+            st.wait -= 1
+            continue
+        if not speculates:
+            continue
+        if kept[b] > 0:
+            st.misses = 0  # forgets to set the wait back to 16
+            continue
+        st.misses += 1
+        if st.misses == ob.MISSES_TO_WAIT:
+            st.wait, st.backoff, st.misses = st.backoff, min(2 * st.backoff, ob.LONGEST_WAIT), 0
+    return [ob.may_guess(st) for st in states]
+
+
+@pytest.mark.parametrize("bad,check", [(_step_counts_every_pass, oc.check_backoff_passes_without_speculation),
+                                       (_step_keep_during_run_not_reset, oc.check_backoff_kept_guess_resets)])
+def test_backoff_step_mistakes_are_caught(monkeypatch, bad, check):
+    monkeypatch.setattr(ob, "step", bad)
+    with pytest.raises(AssertionError):
+        check()
 
 
 def test_philox_round_count_matters(monkeypatch):
