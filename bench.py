@@ -65,10 +65,14 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The files the verify and commit kernels are built from (the profiled kernels).
+KERNEL_SOURCES = ["commit_kernel.cuh", "device_ptx.cuh", "philox.cuh", "spec_verify.cu", "verify_kernel.cuh"]
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verify_bf16_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     with open(os.path.join(ROOT, "include", "spec_verify.h"), "rb") as f:
@@ -448,10 +452,53 @@ def run_ours(args):
         line["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
     if rank == 0 and args.all_workloads:
         line["workloads"] = other_workloads(args, device, stream, peak)
+        line["round_control"] = round_control_timing(device, stream)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def round_control_timing(device, stream, reps=500):
+    """Per-round cost of the acceptance counts and the miss back-off (two tiny
+    kernels a serving loop runs after each verify round), replayed in graphs.
+    Both read ~12 bytes per lane, so they are bound by launch latency, not HBM."""
+    import speculative_decoding_verify_bf16_gb300 as sv
+    out = {}
+    for lanes in (128, 4096):
+        g = torch.Generator(device="cpu").manual_seed(lanes)
+        k = torch.randint(0, 8, (lanes,), generator=g, dtype=torch.int32)
+        committed = (torch.rand(lanes, generator=g) * (k + 1).float()).to(torch.int32) + 1
+        k, committed = k.to(device), committed.to(device)
+        status = torch.zeros(lanes, dtype=torch.int32, device=device)
+        counts = sv.new_accept_counts(1, device)
+        states = sv.new_backoff_states(lanes, device)
+        nxt = torch.empty(lanes, dtype=torch.int32, device=device)
+        entry = {}
+        for name, fn in (("accept_counts_us", lambda: sv.spec_accept_counts_update(committed, k, status, counts,
+                                                                                   stream=stream)),
+                         ("backoff_step_us", lambda: sv.spec_backoff_step(states, k, committed, status, 7, nxt,
+                                                                          stream=stream))):
+            with torch.cuda.stream(stream):
+                fn()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(graph, stream=stream):
+                    for _ in range(reps):
+                        fn()
+            graph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            entry[name] = e0.elapsed_time(e1) * 1e3 / reps
+        entry["bound"] = "launch latency"
+        out[f"lanes_{lanes}"] = entry
+    return out
 
 
 def other_workloads(args, device, stream, peak):

@@ -1,0 +1,121 @@
+/*
+ * spec_round_control.h -- what is done with a verify round's outputs across
+ * rounds: acceptance metrics and the per-lane miss back-off of a drafter.
+ *
+ * Both consume the per-lane outputs of spec_verify_accept (committed counts,
+ * the draft lengths the round used, lane_status) and run on the GPU next to it,
+ * so a serving loop never copies them to the host to keep its books.  The
+ * conventions of spec_verify.h hold: device pointers unless stated otherwise,
+ * caller-owned buffers, calls enqueue on `stream` and return at once.
+ */
+#ifndef SPEC_ROUND_CONTROL_H
+#define SPEC_ROUND_CONTROL_H
+
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Acceptance counts (strata->signal, "Draft heads and speculative decoding, in
+ * plain words" -- "Acceptance: three numbers with one name").  A round of one
+ * lane proposes k guesses and keeps the first n = committed - 1 of them.
+ */
+typedef struct {
+  uint64_t rounds;                         /* rounds counted                               */
+  uint64_t proposed;                       /* sum of k: guesses proposed                   */
+  uint64_t accepted;                       /* sum of n: guesses kept                       */
+  uint64_t slot_reached[SPEC_MAX_DRAFTS];  /* [j]: rounds that proposed guess j + 1 (k > j) */
+  uint64_t slot_kept[SPEC_MAX_DRAFTS];     /* [j]: rounds in which guess j + 1 survived (n > j) */
+} spec_accept_counts;                      /* 264 bytes */
+
+/*
+ * spec_accept_counts_update -- add one verify round to the counts.
+ *
+ * Lane b proposed draft_lens[b] guesses and committed committed[b] tokens.
+ * Lanes whose lane_status is not SPEC_OK (lane_status may be NULL: all lanes
+ * OK), whose draft length is outside 0..SPEC_MAX_DRAFTS or whose committed
+ * count is outside 1..draft_lens[b] + 1 are left out.  per_lane = 0 adds every
+ * lane into counts[0] (one struct for the batch); per_lane = 1 adds lane b into
+ * counts[b] (counts has `lanes` entries).  counts is device memory the caller
+ * zero-fills before the first round.  Reads nothing written by the host in the
+ * same call, so it may follow spec_verify_accept on the same stream directly.
+ *
+ * Errors: SPEC_ERR_INVALID_ARG for NULL committed / draft_lens / counts with
+ * lanes > 0, lanes < 0 or per_lane not 0 or 1; SPEC_ERR_CUDA if the launch
+ * fails.
+ */
+int spec_accept_counts_update(const int32_t* committed, const int32_t* draft_lens, const int32_t* lane_status,
+                              int32_t lanes, spec_accept_counts* counts, int32_t per_lane, void* stream);
+
+/* The page's quantities, from a set of counts. */
+typedef struct {
+  double accepted_per_proposed;            /* accepted / proposed                          */
+  double tokens_per_round;                 /* 1 + accepted / rounds                        */
+  double by_slot[SPEC_MAX_DRAFTS];         /* slot_kept[j] / rounds                        */
+  double given_previous[SPEC_MAX_DRAFTS];  /* slot_kept[j] / slot_kept[j - 1] (j = 0: / rounds) */
+  int32_t depth;                           /* proposed / rounds, rounded: the alpha's depth g */
+  int32_t reserved;
+  double implied_alpha;                    /* alpha in [0, 1] with
+                                              (1 - alpha^(g + 1)) / (1 - alpha) = tokens_per_round */
+} spec_accept_rates;
+
+/*
+ * spec_accept_rates_from_counts -- derive the rates (host-only, both pointers
+ * host memory).  A ratio with a zero denominator is NaN.  Returns
+ * SPEC_ERR_INVALID_ARG for a NULL pointer, SPEC_OK otherwise.
+ */
+int spec_accept_rates_from_counts(const spec_accept_counts* counts, spec_accept_rates* rates);
+
+/*
+ * Miss back-off (mashbox docs, "Speculative decoding" -- "What it does for
+ * you"): after 4 counted passes in a row in which the model kept none of a
+ * lane's guesses the lane makes no guesses for 16 passes; each further 4 such
+ * passes in a row double the wait, up to 256; a pass that keeps a guess sets
+ * the wait back to 16.  One verify round is one pass of one device call: a
+ * round in which no lane of the batch proposed a guess counts toward no lane's
+ * misses, only toward the wait of a lane already waiting, and in a round that
+ * speculates every lane that may guess counts, with or without a guess.
+ */
+typedef struct {
+  int32_t misses;   /* counted passes in a row in which no guess was kept */
+  int32_t backoff;  /* length of the next wait, 16 .. 256                 */
+  int32_t wait;     /* passes left in the current wait; 0: the lane may guess */
+  int32_t reserved;
+} spec_backoff_state;
+
+/*
+ * spec_backoff_init -- state of `lanes` lanes that have not missed yet
+ * (misses 0, backoff 16, wait 0).  Errors: SPEC_ERR_INVALID_ARG for a NULL
+ * `states` with lanes > 0 or lanes < 0; SPEC_ERR_CUDA if the launch fails.
+ */
+int spec_backoff_init(spec_backoff_state* states, int32_t lanes, void* stream);
+
+/*
+ * spec_backoff_step -- advance every lane by one verify round and write the
+ * draft length each lane may use in the next round.
+ *
+ * proposed[b] is the draft length lane b used in the round (0 while it was
+ * waiting); the round kept committed[b] - 1 of its guesses.  A lane whose
+ * lane_status is not SPEC_OK (lane_status may be NULL) kept none.  The lane's
+ * next draft length is draft_tokens (0 <= draft_tokens <= SPEC_MAX_DRAFTS)
+ * unless it is waiting, then 0; next_draft_lens may be the array the next
+ * round reads as draft_lens.  One CTA walks all lanes (the round-level
+ * "did any lane guess" needs the whole batch).
+ *
+ * Errors: SPEC_ERR_INVALID_ARG for NULL pointers (other than lane_status) with
+ * lanes > 0, lanes < 0 or draft_tokens outside 0..SPEC_MAX_DRAFTS;
+ * SPEC_ERR_CUDA if the launch fails.
+ */
+int spec_backoff_step(spec_backoff_state* states, const int32_t* proposed, const int32_t* committed,
+                      const int32_t* lane_status, int32_t lanes, int32_t draft_tokens, int32_t* next_draft_lens,
+                      void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_ROUND_CONTROL_H */

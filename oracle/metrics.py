@@ -53,12 +53,16 @@ def count_round(counts, k, n):
 
 def count_verify_outputs(counts, committed, draft_lens, lane_status=None):
     """Add one verify round's outputs: lane b proposed draft_lens[b] and
-    committed committed[b] = kept + 1 tokens.  Lanes whose status is not 0 are
-    left out."""
+    committed committed[b] = kept + 1 tokens.  Lanes whose status is not 0, or
+    whose counts are not a verify result (draft length outside 0..15, committed
+    outside 1..draft length + 1), are left out."""
     for b in range(len(committed)):
         if lane_status is not None and lane_status[b] != 0:
             continue
-        count_round(counts, int(draft_lens[b]), int(committed[b]) - 1)
+        k, c = int(draft_lens[b]), int(committed[b])
+        if not (0 <= k <= MAX_SLOTS and 1 <= c <= k + 1):
+            continue
+        count_round(counts, k, c - 1)
     return counts
 
 

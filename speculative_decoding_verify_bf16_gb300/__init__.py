@@ -20,6 +20,8 @@ __all__ = [
     "SPEC_MAX_DRAFTS", "SpecError", "ROW_STATS_FIELDS", "load_library", "build_library",
     "spec_row_budget", "spec_verify_accept", "spec_commit_state", "spec_status_string",
     "spec_verify_launch_shape", "spec_round_uniforms", "new_row_stats", "row_stats_view",
+    "spec_accept_counts_update", "spec_accept_rates_from_counts", "new_accept_counts", "accept_counts_view",
+    "spec_backoff_step", "new_backoff_states", "BACKOFF_FIELDS", "ACCEPT_COUNT_WORDS",
 ]
 
 SPEC_OK = 0
@@ -72,6 +74,21 @@ class _Args(ctypes.Structure):
 _lib = None
 
 
+class _AcceptCounts(ctypes.Structure):
+    _fields_ = [("rounds", ctypes.c_uint64), ("proposed", ctypes.c_uint64), ("accepted", ctypes.c_uint64),
+                ("slot_reached", ctypes.c_uint64 * SPEC_MAX_DRAFTS), ("slot_kept", ctypes.c_uint64 * SPEC_MAX_DRAFTS)]
+
+
+class _AcceptRates(ctypes.Structure):
+    _fields_ = [("accepted_per_proposed", ctypes.c_double), ("tokens_per_round", ctypes.c_double),
+                ("by_slot", ctypes.c_double * SPEC_MAX_DRAFTS), ("given_previous", ctypes.c_double * SPEC_MAX_DRAFTS),
+                ("depth", ctypes.c_int32), ("reserved", ctypes.c_int32), ("implied_alpha", ctypes.c_double)]
+
+
+ACCEPT_COUNT_WORDS = 3 + 2 * SPEC_MAX_DRAFTS
+BACKOFF_FIELDS = ("misses", "backoff", "wait", "reserved")
+
+
 def load_library():
     """Load libspecverify.so (built in-tree); raise if it is missing."""
     global _lib
@@ -98,6 +115,16 @@ def load_library():
     lib.spec_verify_launch_shape.restype = ctypes.c_int
     lib.spec_verify_launch_shape.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int] + \
         [ctypes.POINTER(ctypes.c_int32)] * 4
+    lib.spec_accept_counts_update.restype = ctypes.c_int
+    lib.spec_accept_counts_update.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                              ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
+    lib.spec_accept_rates_from_counts.restype = ctypes.c_int
+    lib.spec_accept_rates_from_counts.argtypes = [ctypes.POINTER(_AcceptCounts), ctypes.POINTER(_AcceptRates)]
+    lib.spec_backoff_init.restype = ctypes.c_int
+    lib.spec_backoff_init.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
+    lib.spec_backoff_step.restype = ctypes.c_int
+    lib.spec_backoff_step.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
     _lib = lib
     return lib
 
@@ -287,3 +314,78 @@ def spec_verify_launch_shape(lanes, rows, V, dtype=torch.bfloat16):
     if code != SPEC_OK:
         raise SpecError(code, "spec_verify_launch_shape")
     return dict(zip(("cluster_ctas", "threads", "slice", "smem_bytes"), (v.value for v in vals)))
+
+
+# ---------------------------------------------------------------------------
+# Acceptance metrics and miss back-off (include/spec_round_control.h)
+# ---------------------------------------------------------------------------
+def new_accept_counts(n, device):
+    """Zeroed int64 [n, 33] buffer laid out as n spec_accept_counts."""
+    return torch.zeros(n, ACCEPT_COUNT_WORDS, dtype=torch.int64, device=device)
+
+
+def accept_counts_view(row):
+    """Dict of one spec_accept_counts row (any int64 tensor or sequence of 33 words)."""
+    w = [int(x) for x in (row.tolist() if isinstance(row, torch.Tensor) else row)]
+    k = SPEC_MAX_DRAFTS
+    return {"rounds": w[0], "proposed": w[1], "accepted": w[2],
+            "slot_reached": w[3:3 + k], "slot_kept": w[3 + k:3 + 2 * k]}
+
+
+def spec_accept_counts_update(committed, draft_lens, lane_status, counts, per_lane=False, stream=None):
+    """Add one verify round's outputs to device counts (new_accept_counts(1) for the
+    batch, new_accept_counts(lanes) with per_lane=True)."""
+    lib = load_library()
+    dev = committed.device
+    lanes = committed.numel()
+    _need(committed, "committed", torch.int32, dev)
+    _need(draft_lens, "draft_lens", torch.int32, dev, lanes)
+    if lane_status is not None:
+        _need(lane_status, "lane_status", torch.int32, dev, lanes)
+    _need(counts, "counts", torch.int64, dev, (lanes if per_lane else 1) * ACCEPT_COUNT_WORDS)
+    rc = lib.spec_accept_counts_update(_ptr(committed), _ptr(draft_lens), _ptr(lane_status), lanes,
+                                       _ptr(counts), 1 if per_lane else 0, _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_accept_counts_update")
+
+
+def spec_accept_rates_from_counts(counts_row):
+    """The page's rates from one set of counts (host call)."""
+    c = accept_counts_view(counts_row)
+    cs = _AcceptCounts(c["rounds"], c["proposed"], c["accepted"],
+                       (ctypes.c_uint64 * SPEC_MAX_DRAFTS)(*c["slot_reached"]),
+                       (ctypes.c_uint64 * SPEC_MAX_DRAFTS)(*c["slot_kept"]))
+    r = _AcceptRates()
+    rc = load_library().spec_accept_rates_from_counts(ctypes.byref(cs), ctypes.byref(r))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_accept_rates_from_counts")
+    return {"accepted_per_proposed": r.accepted_per_proposed, "tokens_per_round": r.tokens_per_round,
+            "by_slot": list(r.by_slot), "given_previous": list(r.given_previous), "depth": r.depth,
+            "implied_alpha": r.implied_alpha}
+
+
+def new_backoff_states(lanes, device, stream=None):
+    """int32 [lanes, 4] back-off states, initialised on the device."""
+    st = torch.empty(lanes, 4, dtype=torch.int32, device=device)
+    rc = load_library().spec_backoff_init(_ptr(st), lanes, _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_backoff_init")
+    return st
+
+
+def spec_backoff_step(states, proposed, committed, lane_status, draft_tokens, next_draft_lens, stream=None):
+    """Advance the back-off of every lane by one verify round; writes the next
+    round's draft lengths."""
+    lib = load_library()
+    dev = states.device
+    lanes = proposed.numel()
+    _need(states, "states", torch.int32, dev, lanes * 4)
+    _need(proposed, "proposed", torch.int32, dev)
+    _need(committed, "committed", torch.int32, dev, lanes)
+    if lane_status is not None:
+        _need(lane_status, "lane_status", torch.int32, dev, lanes)
+    _need(next_draft_lens, "next_draft_lens", torch.int32, dev, lanes)
+    rc = lib.spec_backoff_step(_ptr(states), _ptr(proposed), _ptr(committed), _ptr(lane_status), lanes,
+                               int(draft_tokens), _ptr(next_draft_lens), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_backoff_step")

@@ -20,8 +20,12 @@ NVCC_FLAGS = [
 
 def _sources():
     files = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))]
-    files.append(os.path.join(INCLUDE, "spec_verify.h"))
+    files += [os.path.join(INCLUDE, f) for f in sorted(os.listdir(INCLUDE)) if f.endswith(".h")]
     return files
+
+
+def _translation_units():
+    return [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith(".cu")]
 
 
 def _nvcc():
@@ -39,11 +43,12 @@ def up_to_date():
 
 
 def build_library(force=False, verbose=False):
-    """Compile csrc/spec_verify.cu into the package directory; return the path."""
+    """Compile the csrc/*.cu translation units into one library in the package
+    directory; return its path."""
     if not force and up_to_date():
         return LIB_PATH
     tmp = LIB_PATH + ".tmp"
-    cmd = [_nvcc(), *NVCC_FLAGS, "-I" + INCLUDE, "-o", tmp, os.path.join(CSRC, "spec_verify.cu")]
+    cmd = [_nvcc(), *NVCC_FLAGS, "-I" + INCLUDE, "-o", tmp, *_translation_units()]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     res = subprocess.run(cmd, capture_output=True, text=True)

@@ -1,0 +1,201 @@
+// round_control.cu -- acceptance counts and the per-lane miss back-off, the C
+// ABI of include/spec_round_control.h.  Both read a verify round's per-lane
+// outputs on the device; neither allocates memory.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "spec_round_control.h"
+
+namespace {
+
+constexpr int kSlots = SPEC_MAX_DRAFTS;
+constexpr int kCountWords = 3 + 2 * kSlots;  // spec_accept_counts as 64-bit words
+static_assert(sizeof(spec_accept_counts) == kCountWords * 8, "spec_accept_counts layout");
+
+constexpr int kMissesToWait = 4;   // passes in a row with nothing kept before a wait
+constexpr int kFirstWait = 16;     // passes of the first wait
+constexpr int kLongestWait = 256;  // the wait doubles up to this
+
+// Whether lane b's round is counted, and its guesses proposed (k) and kept (n).
+__device__ __forceinline__ bool lane_round(const int32_t* committed, const int32_t* draft_lens,
+                                           const int32_t* lane_status, int b, int& k, int& n) {
+  if (lane_status != nullptr && lane_status[b] != SPEC_OK) return false;
+  k = draft_lens[b];
+  const int c = committed[b];
+  if (k < 0 || k > kSlots || c < 1 || c > k + 1) return false;
+  n = c - 1;
+  return true;
+}
+
+// The whole batch into one struct: per-thread partial counts, then warp sums,
+// shared-memory sums per CTA and one 64-bit atomic per word and CTA.
+__global__ void __launch_bounds__(256) accept_counts_batch_kernel(const int32_t* committed,
+                                                                  const int32_t* draft_lens,
+                                                                  const int32_t* lane_status, int32_t lanes,
+                                                                  unsigned long long* out) {
+  __shared__ unsigned long long tot[kCountWords];
+  for (int i = threadIdx.x; i < kCountWords; i += blockDim.x) tot[i] = 0ull;
+  __syncthreads();
+  unsigned int part[kCountWords];
+#pragma unroll
+  for (int i = 0; i < kCountWords; ++i) part[i] = 0u;
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < lanes; b += gridDim.x * blockDim.x) {
+    int k, n;
+    if (!lane_round(committed, draft_lens, lane_status, b, k, n)) continue;
+    part[0] += 1u;
+    part[1] += static_cast<unsigned int>(k);
+    part[2] += static_cast<unsigned int>(n);
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j) {
+      part[3 + j] += (k > j) ? 1u : 0u;
+      part[3 + kSlots + j] += (n > j) ? 1u : 0u;
+    }
+  }
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < kCountWords; ++i) {
+    const unsigned int w = __reduce_add_sync(0xFFFFFFFFu, part[i]);
+    if (lane == 0 && w != 0u) atomicAdd(&tot[i], static_cast<unsigned long long>(w));
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kCountWords; i += blockDim.x)
+    if (tot[i] != 0ull) atomicAdd(&out[i], tot[i]);
+}
+
+// Lane b into counts[b] (one thread per lane owns its struct).
+__global__ void accept_counts_lane_kernel(const int32_t* committed, const int32_t* draft_lens,
+                                          const int32_t* lane_status, int32_t lanes, unsigned long long* out) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= lanes) return;
+  int k, n;
+  if (!lane_round(committed, draft_lens, lane_status, b, k, n)) return;
+  unsigned long long* c = out + static_cast<int64_t>(b) * kCountWords;
+  c[0] += 1ull;
+  c[1] += static_cast<unsigned long long>(k);
+  c[2] += static_cast<unsigned long long>(n);
+  for (int j = 0; j < k; ++j) c[3 + j] += 1ull;
+  for (int j = 0; j < n; ++j) c[3 + kSlots + j] += 1ull;
+}
+
+__global__ void backoff_init_kernel(spec_backoff_state* states, int32_t lanes) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < lanes) states[b] = spec_backoff_state{0, kFirstWait, 0, 0};
+}
+
+// One pass for every lane (mashbox docs, "Speculative decoding" -- "What it
+// does for you"), read with one pass per device call.  A single CTA: first
+// whether any lane of the batch guessed (a round that does not speculate
+// counts toward no miss run), then each lane's state.
+__global__ void __launch_bounds__(1024) backoff_step_kernel(spec_backoff_state* states, const int32_t* proposed,
+                                                            const int32_t* committed, const int32_t* lane_status,
+                                                            int32_t lanes, int32_t draft_tokens,
+                                                            int32_t* next_draft_lens) {
+  int guessed = 0;
+  for (int b = threadIdx.x; b < lanes; b += blockDim.x) guessed |= (proposed[b] > 0) ? 1 : 0;
+  const bool speculates = __syncthreads_or(guessed) != 0;
+  for (int b = threadIdx.x; b < lanes; b += blockDim.x) {
+    spec_backoff_state s = states[b];
+    if (s.wait > 0) {
+      s.wait -= 1;  // every pass of a waiting lane counts toward its wait
+    } else if (speculates) {
+      const bool ok = (lane_status == nullptr || lane_status[b] == SPEC_OK);
+      const bool kept = ok && proposed[b] > 0 && committed[b] > 1;
+      if (kept) {
+        s.misses = 0;
+        s.backoff = kFirstWait;
+      } else if (++s.misses == kMissesToWait) {
+        s.wait = s.backoff;
+        s.backoff = min(2 * s.backoff, kLongestWait);
+        s.misses = 0;
+      }
+    }
+    states[b] = s;
+    next_draft_lens[b] = (s.wait > 0) ? 0 : draft_tokens;
+  }
+}
+
+int launch_status() { return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
+
+// (1 - alpha^(g + 1)) / (1 - alpha): expected tokens a round of independent
+// guesses that each survive with probability alpha, at depth g.
+double tokens_of_alpha(double alpha, int depth) {
+  if (alpha >= 1.0) return depth + 1.0;
+  return (1.0 - std::pow(alpha, depth + 1)) / (1.0 - alpha);
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_accept_counts_update(const int32_t* committed, const int32_t* draft_lens, const int32_t* lane_status,
+                              int32_t lanes, spec_accept_counts* counts, int32_t per_lane, void* stream) {
+  if (lanes < 0 || (per_lane != 0 && per_lane != 1)) return SPEC_ERR_INVALID_ARG;
+  if (lanes == 0) return SPEC_OK;
+  if (committed == nullptr || draft_lens == nullptr || counts == nullptr) return SPEC_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned long long* out = reinterpret_cast<unsigned long long*>(counts);
+  const int blocks = (lanes + 255) / 256;
+  if (per_lane) {
+    accept_counts_lane_kernel<<<blocks, 256, 0, st>>>(committed, draft_lens, lane_status, lanes, out);
+  } else {
+    accept_counts_batch_kernel<<<blocks < 148 ? blocks : 148, 256, 0, st>>>(committed, draft_lens, lane_status,
+                                                                             lanes, out);
+  }
+  return launch_status();
+}
+
+int spec_accept_rates_from_counts(const spec_accept_counts* c, spec_accept_rates* r) {
+  if (c == nullptr || r == nullptr) return SPEC_ERR_INVALID_ARG;
+  const double rounds = static_cast<double>(c->rounds);
+  r->accepted_per_proposed = c->proposed ? static_cast<double>(c->accepted) / c->proposed : NAN;
+  r->tokens_per_round = c->rounds ? 1.0 + static_cast<double>(c->accepted) / rounds : NAN;
+  double prev = rounds;
+  for (int j = 0; j < kSlots; ++j) {
+    r->by_slot[j] = c->rounds ? static_cast<double>(c->slot_kept[j]) / rounds : NAN;
+    r->given_previous[j] = prev > 0 ? static_cast<double>(c->slot_kept[j]) / prev : NAN;
+    prev = static_cast<double>(c->slot_kept[j]);
+  }
+  r->depth = c->rounds ? static_cast<int32_t>(static_cast<double>(c->proposed) / rounds + 0.5) : 0;
+  r->reserved = 0;
+  // Bisection on [0, 1]: the expected tokens a round grow with alpha.
+  if (!c->rounds || r->depth <= 0) {
+    r->implied_alpha = NAN;
+  } else if (r->tokens_per_round <= 1.0) {
+    r->implied_alpha = 0.0;
+  } else if (r->tokens_per_round >= r->depth + 1.0) {
+    r->implied_alpha = 1.0;
+  } else {
+    double lo = 0.0, hi = 1.0;
+    for (int it = 0; it < 200; ++it) {
+      const double mid = 0.5 * (lo + hi);
+      if (tokens_of_alpha(mid, r->depth) < r->tokens_per_round) lo = mid;
+      else hi = mid;
+    }
+    r->implied_alpha = 0.5 * (lo + hi);
+  }
+  return SPEC_OK;
+}
+
+int spec_backoff_init(spec_backoff_state* states, int32_t lanes, void* stream) {
+  if (lanes < 0) return SPEC_ERR_INVALID_ARG;
+  if (lanes == 0) return SPEC_OK;
+  if (states == nullptr) return SPEC_ERR_INVALID_ARG;
+  backoff_init_kernel<<<(lanes + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(states, lanes);
+  return launch_status();
+}
+
+int spec_backoff_step(spec_backoff_state* states, const int32_t* proposed, const int32_t* committed,
+                      const int32_t* lane_status, int32_t lanes, int32_t draft_tokens, int32_t* next_draft_lens,
+                      void* stream) {
+  if (lanes < 0 || draft_tokens < 0 || draft_tokens > SPEC_MAX_DRAFTS) return SPEC_ERR_INVALID_ARG;
+  if (lanes == 0) return SPEC_OK;
+  if (states == nullptr || proposed == nullptr || committed == nullptr || next_draft_lens == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  backoff_step_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(states, proposed, committed, lane_status,
+                                                                        lanes, draft_tokens, next_draft_lens);
+  return launch_status();
+}
+
+}  // extern "C"

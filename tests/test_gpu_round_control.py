@@ -1,0 +1,136 @@
+"""Acceptance counts and the miss back-off on the GPU against the oracle (integers: exact)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_checks as oc
+import workloads
+from conftest import read_golden
+from gpu_harness import run_gpu
+from oracle import backoff as ob
+from oracle import metrics as om
+
+import speculative_decoding_verify_bf16_gb300 as sv
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+def _row(c):
+    return [c.rounds, c.proposed, c.accepted] + list(c.slot_reached) + list(c.slot_kept)
+
+
+def _i32(a):
+    return torch.tensor(np.asarray(a, np.int32), device=DEV)
+
+
+def test_counts_of_verify_rounds_match_the_oracle():
+    """Several verify rounds of mixed lanes, counted on the GPU per batch and per
+    lane, equal the oracle's counts of the same outputs."""
+    lanes = 24
+    batch = sv.new_accept_counts(1, DEV)
+    per_lane = sv.new_accept_counts(lanes, DEV)
+    orc_batch = om.AcceptCounts()
+    orc_lane = [om.AcceptCounts() for _ in range(lanes)]
+    for seed in range(6):
+        r = workloads.make_custom_round(300 + seed, DEV, lanes=lanes, vocab=20000, kmax=7, dtype="bf16",
+                                        sampled="mixed")
+        g = run_gpu(r, stats=False)
+        committed = _i32(g["committed"])
+        status = _i32(g["lane_status"])
+        sv.spec_accept_counts_update(committed, r.draft_lens, status, batch)
+        sv.spec_accept_counts_update(committed, r.draft_lens, status, per_lane, per_lane=True)
+        k = r.draft_lens.cpu().numpy()
+        om.count_verify_outputs(orc_batch, g["committed"], k, g["lane_status"])
+        for b in range(lanes):
+            om.count_verify_outputs(orc_lane[b], g["committed"][b:b + 1], k[b:b + 1], g["lane_status"][b:b + 1])
+    torch.cuda.synchronize()
+    assert batch[0].tolist() == _row(orc_batch)
+    for b in range(lanes):
+        assert per_lane[b].tolist() == _row(orc_lane[b]), b
+    # the per-lane counts add up to the batch's
+    assert per_lane.sum(0).tolist() == batch[0].tolist()
+
+
+def test_counts_skip_failed_and_impossible_lanes():
+    rng = np.random.default_rng(3)
+    lanes = 5000
+    k = rng.integers(-2, 18, lanes)
+    committed = rng.integers(-1, 20, lanes)
+    status = np.where(rng.random(lanes) < 0.1, oracle.STATUS_NONFINITE, 0)
+    for st in (status, None):
+        counts = sv.new_accept_counts(1, DEV)
+        sv.spec_accept_counts_update(_i32(committed), _i32(k), None if st is None else _i32(st), counts)
+        torch.cuda.synchronize()
+        want = om.count_verify_outputs(om.AcceptCounts(), committed, k, st)
+        assert counts[0].tolist() == _row(want)
+        assert want.rounds > 1000
+
+
+def test_worked_example_through_the_device_counts():
+    ks, ns = [], []
+    for k, n, times in read_golden("acceptance_rounds_worked_example.txt"):
+        ks += [k] * times
+        ns += [n] * times
+    counts = sv.new_accept_counts(1, DEV)
+    sv.spec_accept_counts_update(_i32(np.array(ns) + 1), _i32(ks), None, counts)
+    torch.cuda.synchronize()
+    c = sv.accept_counts_view(counts[0])
+    assert (c["rounds"], c["proposed"], c["accepted"]) == (43, 171, 84)
+    r = sv.spec_accept_rates_from_counts(counts[0])
+    g = oc._golden_rates()
+    oc._printed(r["accepted_per_proposed"], g["accepted_per_proposed"])
+    oc._printed(r["tokens_per_round"], g["tokens_per_round"])
+    for j in range(4):
+        oc._printed(r["by_slot"][j], g[f"by_slot_{j + 1}"])
+        oc._printed(r["given_previous"][j], g[f"given_previous_{j + 1}"])
+    oc._printed(r["implied_alpha"], g["implied_alpha"])
+
+
+@pytest.mark.parametrize("lanes,draft_tokens,p_keep", [(64, 3, 0.15), (3000, 5, 0.4), (7, 8, 0.02)])
+def test_backoff_matches_the_oracle_pass_by_pass(lanes, draft_tokens, p_keep):
+    """Random rounds: lanes that may guess sometimes have no guess, some rounds
+    nobody guesses, some lanes fail; states and next draft lengths equal the
+    oracle's after every pass."""
+    rng = np.random.default_rng(lanes)
+    states = sv.new_backoff_states(lanes, DEV)
+    orc = [ob.BackoffState() for _ in range(lanes)]
+    nxt = torch.full((lanes,), draft_tokens, dtype=torch.int32, device=DEV)
+    may = np.full(lanes, draft_tokens)
+    waited = 0
+    for it in range(2000):
+        prop = may.copy()
+        prop[rng.random(lanes) < 0.1] = 0           # the drafter found nothing
+        if rng.random() < 0.05:
+            prop[:] = 0                             # a round in which nobody guesses
+        kept = np.where(rng.random(lanes) < p_keep, rng.integers(1, draft_tokens + 1, lanes), 0)
+        kept = np.minimum(kept, prop)
+        committed = kept + 1
+        status = np.where(rng.random(lanes) < 0.02, oracle.STATUS_NONFINITE, 0)
+        kept_orc = np.where(status == 0, kept, 0)
+        sv.spec_backoff_step(states, _i32(prop), _i32(committed), _i32(status), draft_tokens, nxt)
+        ob.step(orc, prop.tolist(), kept_orc.tolist())
+        may = np.array(ob.next_draft_lens(orc, draft_tokens))
+        if it % 50 == 49 or it == 1999:
+            got = states.cpu().numpy()
+            want = np.array([[s.misses, s.backoff, s.wait] for s in orc])
+            np.testing.assert_array_equal(got[:, :3], want, err_msg=f"pass {it}")
+        np.testing.assert_array_equal(nxt.cpu().numpy(), may, err_msg=f"pass {it}")
+        waited += int((may == 0).sum())
+    assert waited > 0  # waits happened
+
+
+def test_round_control_argument_errors():
+    lib = sv.load_library()
+    assert lib.spec_accept_counts_update(None, None, None, -1, None, 0, None) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_accept_counts_update(None, None, None, 4, None, 0, None) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_accept_counts_update(None, None, None, 0, None, 2, None) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_accept_counts_update(None, None, None, 0, None, 0, None) == sv.SPEC_OK
+    assert lib.spec_backoff_init(None, 3, None) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_backoff_step(None, None, None, None, 3, 2, None, None) == sv.SPEC_ERR_INVALID_ARG
+    st = sv.new_backoff_states(2, DEV)
+    z = torch.zeros(2, dtype=torch.int32, device=DEV)
+    with pytest.raises(sv.SpecError):
+        sv.spec_backoff_step(st, z, z, None, 16, z)
