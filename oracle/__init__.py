@@ -7,9 +7,10 @@ CPU-baseline / reference leg of ``bench.py`` may import it.  It shares no code
 with the CUDA library (no kernels, headers, helpers or constant tables) and
 never calls it; the product path never calls this package.
 
-``oracle.metrics`` counts the acceptance metrics of verify rounds and
-``oracle.backoff`` is the per-lane miss back-off of a drafter; both are plain
-Python restatements of the pages' rules.
+``oracle.metrics`` counts the acceptance metrics of verify rounds,
+``oracle.backoff`` is the per-lane miss back-off of a drafter and
+``oracle.ngram`` the copy-from-the-conversation drafter; all are plain Python
+restatements of the pages' rules.
 
 Every function is pinned by ``-m "not gpu"`` tests against facts fixed outside
 the oracle itself: the pages' worked examples, exact enumeration of the
@@ -17,7 +18,7 @@ acceptance rule on tiny vocabularies, a closed form, library routines (numpy's
 Philox4x64, scipy's softmax / logsumexp) and invariants.
 """
 
-from . import backoff, metrics
+from . import backoff, metrics, ngram
 from .philox import philox4x64_10, round_uniforms, word_to_uniform
 from .verify import (
     DEFAULT_ROW_BUDGET,

@@ -569,6 +569,50 @@ def check_backoff_passes_without_speculation():
     assert ob.next_draft_lens(s, 5) == [0, 5]
 
 
+# ---------------------------------------------------------------------------
+# n-gram drafter: mashbox "Speculative decoding", "Options" (--speculation ngram)
+# ---------------------------------------------------------------------------
+from oracle import ngram as ong
+
+
+def check_ngram_hand_examples():
+    """Worked by hand from the definition: find the last tokens earlier in the
+    history, propose what followed them there."""
+    # "1 2" recurs at positions 1-2; what followed was 3 9 1
+    assert ong.ngram_draft([5, 1, 2, 3, 9, 1, 2], 3)[:2] == ([3, 9, 1], 2)
+    # the last token never occurred before: nothing to propose
+    assert ong.ngram_draft([1, 2, 3], 3)[0] == []
+    # the most recent of two occurrences; only two tokens follow it
+    assert ong.ngram_draft([7, 1, 4, 1, 5, 1], 3)[:3] == ([5, 1], 1, 4)
+    # a longer match wins over a more recent shorter one
+    hist = [1, 2, 3, 8, 2, 3, 9, 1, 2, 3]
+    assert ong.ngram_draft(hist, 3)[:2] == ([8, 2, 3], 3)
+    # ... unless the longest allowed match is shorter
+    assert ong.ngram_draft(hist, 3, match_max=2)[:3] == ([9, 1, 2], 2, 6)
+    # the match may overlap the suffix itself
+    assert ong.ngram_draft([4, 4, 4, 4], 3)[:3] == ([4], 3, 3)
+    # k limits the proposal; a minimum match length can rule a lane out
+    assert ong.ngram_draft([5, 1, 2, 3, 9, 1, 2], 1)[0] == [3]
+    assert ong.ngram_draft([7, 1, 4, 1, 5, 1], 3, match_min=2)[0] == []
+    assert ong.ngram_draft([9], 3)[0] == [] and ong.ngram_draft([1, 1], 0)[0] == []
+
+
+def check_ngram_brute_force(seed=8):
+    """Tiny random histories: the best (length, position) over every earlier
+    occurrence of every allowed suffix, enumerated as a set."""
+    rng = np.random.default_rng(seed)
+    for trial in range(3000):
+        L = int(rng.integers(1, 13))
+        h = [int(x) for x in rng.integers(0, 3, L)]
+        k = int(rng.integers(1, 6))
+        mmin, mmax = sorted(int(x) for x in rng.integers(1, 6, 2))
+        cands = [(m, i) for m in range(mmin, min(mmax, L - 1) + 1) for i in range(m, L)
+                 if h[i - m:i] == h[L - m:]]
+        want = h[max(cands)[1]:max(cands)[1] + k] if cands else []
+        got = ong.ngram_draft(h, k, mmin, mmax)[0]
+        assert got == want, (h, k, mmin, mmax, got, want)
+
+
 ALL_CHECKS = [
     check_row_budget_worked_example,
     check_guess_check_table,
@@ -589,4 +633,6 @@ ALL_CHECKS = [
     check_backoff_waits_16_then_doubles_to_256,
     check_backoff_kept_guess_resets,
     check_backoff_passes_without_speculation,
+    check_ngram_hand_examples,
+    check_ngram_brute_force,
 ]

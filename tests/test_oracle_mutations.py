@@ -183,6 +183,50 @@ def test_backoff_step_mistakes_are_caught(monkeypatch, bad, check):
         check()
 
 
+import oracle.ngram as ong
+
+
+def _ngram_oldest(history, k, match_min=1, match_max=4):
+    h = list(history)
+    L = len(h)
+    if k <= 0 or L < 2:
+        return [], 0, -1
+    for m in range(min(match_max, L - 1), match_min - 1, -1):
+        for i in range(m, L):  # oldest first
+            if h[i - m:i] == h[L - m:]:
+                return h[i:min(i + k, L)], m, i
+    return [], 0, -1
+
+
+def _ngram_shortest(history, k, match_min=1, match_max=4):
+    h = list(history)
+    L = len(h)
+    if k <= 0 or L < 2:
+        return [], 0, -1
+    for m in range(match_min, min(match_max, L - 1) + 1):
+        for i in range(L - 1, m - 1, -1):
+            if h[i - m:i] == h[L - m:]:
+                return h[i:min(i + k, L)], m, i
+    return [], 0, -1
+
+
+def _ngram_includes_match(history, k, match_min=1, match_max=4):
+    d, m, i = _orig_ngram(history, k, match_min, match_max)
+    return (list(history)[i - 1:i - 1 + k], m, i) if i > 0 else (d, m, i)
+
+
+_orig_ngram = ong.ngram_draft
+
+
+@pytest.mark.parametrize("bad", [_ngram_oldest, _ngram_shortest, _ngram_includes_match])
+def test_ngram_mistakes_are_caught(monkeypatch, bad):
+    monkeypatch.setattr(ong, "ngram_draft", bad)
+    with pytest.raises(AssertionError):
+        oc.check_ngram_hand_examples()
+    with pytest.raises(AssertionError):
+        oc.check_ngram_brute_force()
+
+
 def test_philox_round_count_matters(monkeypatch):
     import oracle.philox as ph
     monkeypatch.setattr(ph, "ROUNDS", 9)
