@@ -496,7 +496,33 @@ def round_control_timing(device, stream, reps=500):
                 e1.record(stream)
             torch.cuda.synchronize()
             entry[name] = e0.elapsed_time(e1) * 1e3 / reps
-        entry["bound"] = "launch latency"
+        # n-gram drafter over 2048-token histories of this many lanes
+        hist = 2048
+        toks = torch.randint(0, 512, (lanes * hist,), generator=g, dtype=torch.int32).to(device)
+        offs = (torch.arange(lanes + 1, dtype=torch.int64) * hist).to(device)
+        drafts = torch.empty(lanes, 7, dtype=torch.int32, device=device)
+        lens = torch.empty(lanes, dtype=torch.int32, device=device)
+        fn = lambda: sv.spec_ngram_draft(toks, offs, 7, drafts, lens, stream=stream)
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(reps):
+                    fn()
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        entry["ngram_draft_us"] = e0.elapsed_time(e1) * 1e3 / reps
+        entry["ngram_history_tokens"] = hist
+        entry["bound"] = ("launch latency at 128 lanes; the drafter reads 4 B per history token once (repeats hit L1),"
+                          " so large batches are bound by memory latency")
         out[f"lanes_{lanes}"] = entry
     return out
 

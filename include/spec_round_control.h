@@ -1,10 +1,12 @@
 /*
- * spec_round_control.h -- what is done with a verify round's outputs across
- * rounds: acceptance metrics and the per-lane miss back-off of a drafter.
+ * spec_round_control.h -- the rest of a speculative round around the verify:
+ * acceptance metrics, the per-lane miss back-off of a drafter, and the
+ * copy-from-the-conversation (n-gram) drafter.
  *
- * Both consume the per-lane outputs of spec_verify_accept (committed counts,
- * the draft lengths the round used, lane_status) and run on the GPU next to it,
- * so a serving loop never copies them to the host to keep its books.  The
+ * The first two consume the per-lane outputs of spec_verify_accept (committed
+ * counts, the draft lengths the round used, lane_status), the drafter writes
+ * the next round's drafts; all run on the GPU next to the verify, so a serving
+ * loop never copies a round's results to the host to keep its books.  The
  * conventions of spec_verify.h hold: device pointers unless stated otherwise,
  * caller-owned buffers, calls enqueue on `stream` and return at once.
  */
@@ -113,6 +115,36 @@ int spec_backoff_init(spec_backoff_state* states, int32_t lanes, void* stream);
 int spec_backoff_step(spec_backoff_state* states, const int32_t* proposed, const int32_t* committed,
                       const int32_t* lane_status, int32_t lanes, int32_t draft_tokens, int32_t* next_draft_lens,
                       void* stream);
+
+/* Longest suffix spec_ngram_draft matches. */
+#define SPEC_NGRAM_MAX_MATCH 16
+
+/*
+ * spec_ngram_draft -- copy from the conversation (mashbox docs, "Speculative
+ * decoding" -- "Options", --speculation ngram): look up the last few tokens of
+ * each lane's history earlier in it and propose the tokens that followed them
+ * there.
+ *
+ * Lane b's history is tokens[hist_offsets[b] .. hist_offsets[b + 1]), L tokens
+ * ending with the anchor.  For a match length m the suffix is the last m
+ * tokens; an earlier occurrence of it ends at a position i < L.  The drafter
+ * takes the longest m in [match_min, match_max] (and m < L) that has an earlier
+ * occurrence, the most recent such occurrence (largest i), and proposes the
+ * tokens history[i .. min(i + k, L)).  It writes draft_lens[b] (0 when no
+ * suffix of an allowed length occurs earlier) and drafts[b * draft_stride + j]
+ * for j < draft_lens[b]; the other slots are left as they are.  One CTA per
+ * lane reads the lane's history once (plus up to match_max - 1 repeats of each
+ * token, from L1).
+ *
+ * Errors: SPEC_ERR_INVALID_ARG for NULL pointers with lanes > 0, lanes < 0,
+ * k outside 0..SPEC_MAX_DRAFTS, draft_stride < k, or match lengths outside
+ * 1 <= match_min <= match_max <= SPEC_NGRAM_MAX_MATCH; SPEC_ERR_CUDA if the
+ * launch fails.  Offsets must be non-decreasing (a lane with
+ * hist_offsets[b + 1] < hist_offsets[b] is treated as empty).
+ */
+int spec_ngram_draft(const int32_t* tokens, const int64_t* hist_offsets, int32_t lanes, int32_t k,
+                     int32_t match_min, int32_t match_max, int32_t* drafts, int32_t draft_stride,
+                     int32_t* draft_lens, void* stream);
 
 #ifdef __cplusplus
 }

@@ -22,6 +22,7 @@ __all__ = [
     "spec_verify_launch_shape", "spec_round_uniforms", "new_row_stats", "row_stats_view",
     "spec_accept_counts_update", "spec_accept_rates_from_counts", "new_accept_counts", "accept_counts_view",
     "spec_backoff_step", "new_backoff_states", "BACKOFF_FIELDS", "ACCEPT_COUNT_WORDS",
+    "spec_ngram_draft", "SPEC_NGRAM_MAX_MATCH",
 ]
 
 SPEC_OK = 0
@@ -122,6 +123,9 @@ def load_library():
     lib.spec_accept_rates_from_counts.argtypes = [ctypes.POINTER(_AcceptCounts), ctypes.POINTER(_AcceptRates)]
     lib.spec_backoff_init.restype = ctypes.c_int
     lib.spec_backoff_init.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
+    lib.spec_ngram_draft.restype = ctypes.c_int
+    lib.spec_ngram_draft.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                     ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
     lib.spec_backoff_step.restype = ctypes.c_int
     lib.spec_backoff_step.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
@@ -389,3 +393,25 @@ def spec_backoff_step(states, proposed, committed, lane_status, draft_tokens, ne
                                int(draft_tokens), _ptr(next_draft_lens), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_backoff_step")
+
+
+SPEC_NGRAM_MAX_MATCH = 16
+
+
+def spec_ngram_draft(tokens, hist_offsets, k, drafts, draft_lens, match_min=1, match_max=4, stream=None):
+    """Copy-from-the-conversation drafts for every lane: tokens int32 [total],
+    hist_offsets int64 [lanes + 1], drafts int32 [lanes, >= k] (row stride taken
+    as the draft stride), draft_lens int32 [lanes]."""
+    lib = load_library()
+    dev = tokens.device
+    lanes = hist_offsets.numel() - 1
+    _need(tokens, "tokens", torch.int32, dev)
+    _need(hist_offsets, "hist_offsets", torch.int64, dev, lanes + 1)
+    _need(draft_lens, "draft_lens", torch.int32, dev, lanes)
+    if drafts.dim() != 2 or drafts.dtype != torch.int32 or drafts.device != dev or drafts.stride(1) != 1 \
+            or drafts.shape[0] < lanes:
+        raise ValueError("drafts must be an int32 [lanes, >= k] tensor with unit inner stride")
+    rc = lib.spec_ngram_draft(_ptr(tokens), _ptr(hist_offsets), lanes, int(k), int(match_min), int(match_max),
+                              _ptr(drafts), drafts.stride(0), _ptr(draft_lens), _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_ngram_draft")

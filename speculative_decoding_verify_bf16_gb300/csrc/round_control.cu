@@ -1,6 +1,6 @@
-// round_control.cu -- acceptance counts and the per-lane miss back-off, the C
-// ABI of include/spec_round_control.h.  Both read a verify round's per-lane
-// outputs on the device; neither allocates memory.
+// round_control.cu -- acceptance counts, the per-lane miss back-off and the
+// copy-from-the-conversation drafter: the C ABI of include/spec_round_control.h.
+// All run on the device next to the verify kernel; none allocates memory.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -116,6 +116,57 @@ __global__ void __launch_bounds__(1024) backoff_step_kernel(spec_backoff_state* 
   }
 }
 
+constexpr int kNgramThreads = 256;
+
+// Copy from the conversation (mashbox docs, "Speculative decoding" --
+// "Options", --speculation ngram), one CTA per lane.  Every end position i of
+// the history gets the length of its backward match against the suffix (up to
+// mm tokens); the best is the longest match of at least match_min tokens,
+// latest position on ties, found as the max of (length << 40 | i).
+__global__ void __launch_bounds__(kNgramThreads) ngram_draft_kernel(const int32_t* tokens,
+                                                                   const int64_t* hist_offsets, int32_t k,
+                                                                   int32_t match_min, int32_t match_max,
+                                                                   int32_t* drafts, int32_t draft_stride,
+                                                                   int32_t* draft_lens) {
+  __shared__ int32_t suffix[SPEC_NGRAM_MAX_MATCH];
+  __shared__ unsigned long long best;
+  const int b = blockIdx.x;
+  const int64_t o0 = hist_offsets[b], o1 = hist_offsets[b + 1];
+  const int64_t L = (o1 > o0) ? o1 - o0 : 0;
+  const int32_t* h = tokens + o0;
+  const int mm = static_cast<int>(L - 1 < match_max ? L - 1 : match_max);  // longest usable match
+  if (k == 0 || mm < match_min) {  // nothing can match (includes L < 2)
+    if (threadIdx.x == 0) draft_lens[b] = 0;
+    return;
+  }
+  if (threadIdx.x < mm) suffix[threadIdx.x] = h[L - mm + threadIdx.x];
+  if (threadIdx.x == 0) best = 0ull;
+  __syncthreads();
+  unsigned long long mine = 0ull;
+  // End positions i in [match_min, L - 1]; the match at i compares h[i - 1 - j]
+  // with the suffix's token L - 1 - j.
+  for (int64_t i = match_min + threadIdx.x; i < L; i += kNgramThreads) {
+    const int lim = static_cast<int>(i < mm ? i : mm);
+    int m = 0;
+    while (m < lim && h[i - 1 - m] == suffix[mm - 1 - m]) ++m;
+    if (m >= match_min) {
+      const unsigned long long key = (static_cast<unsigned long long>(m) << 40) | static_cast<unsigned long long>(i);
+      mine = key > mine ? key : mine;
+    }
+  }
+  if (mine != 0ull) atomicMax(&best, mine);
+  __syncthreads();
+  const unsigned long long key = best;
+  if (key == 0ull) {
+    if (threadIdx.x == 0) draft_lens[b] = 0;
+    return;
+  }
+  const int64_t i = static_cast<int64_t>(key & ((1ull << 40) - 1));
+  const int n = static_cast<int>((L - i) < k ? (L - i) : k);
+  if (threadIdx.x < n) drafts[static_cast<int64_t>(b) * draft_stride + threadIdx.x] = h[i + threadIdx.x];
+  if (threadIdx.x == 0) draft_lens[b] = n;
+}
+
 int launch_status() { return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
 
 // (1 - alpha^(g + 1)) / (1 - alpha): expected tokens a round of independent
@@ -195,6 +246,20 @@ int spec_backoff_step(spec_backoff_state* states, const int32_t* proposed, const
     return SPEC_ERR_INVALID_ARG;
   backoff_step_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(states, proposed, committed, lane_status,
                                                                         lanes, draft_tokens, next_draft_lens);
+  return launch_status();
+}
+
+int spec_ngram_draft(const int32_t* tokens, const int64_t* hist_offsets, int32_t lanes, int32_t k,
+                     int32_t match_min, int32_t match_max, int32_t* drafts, int32_t draft_stride,
+                     int32_t* draft_lens, void* stream) {
+  if (lanes < 0 || k < 0 || k > SPEC_MAX_DRAFTS || draft_stride < k || match_min < 1 || match_max < match_min ||
+      match_max > SPEC_NGRAM_MAX_MATCH)
+    return SPEC_ERR_INVALID_ARG;
+  if (lanes == 0) return SPEC_OK;
+  if (tokens == nullptr || hist_offsets == nullptr || drafts == nullptr || draft_lens == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  ngram_draft_kernel<<<lanes, kNgramThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      tokens, hist_offsets, k, match_min, match_max, drafts, draft_stride, draft_lens);
   return launch_status();
 }
 

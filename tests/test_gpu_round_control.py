@@ -1,4 +1,5 @@
-"""Acceptance counts and the miss back-off on the GPU against the oracle (integers: exact)."""
+"""Acceptance counts, the miss back-off and the n-gram drafter on the GPU
+against the oracle (integers: exact)."""
 
 import numpy as np
 import pytest
@@ -134,3 +135,52 @@ def test_round_control_argument_errors():
     z = torch.zeros(2, dtype=torch.int32, device=DEV)
     with pytest.raises(sv.SpecError):
         sv.spec_backoff_step(st, z, z, None, 16, z)
+
+
+# ---------------------------------------------------------------------------
+# copy-from-the-conversation drafter
+# ---------------------------------------------------------------------------
+def _ngram_case(rng, lanes, max_len, vocab):
+    lens = rng.integers(0, max_len + 1, lanes)
+    hists = [[int(x) for x in rng.integers(0, vocab, n)] for n in lens]
+    # plant recurrences so that long matches exist
+    for h in hists:
+        if len(h) > 12 and rng.random() < 0.7:
+            m = int(rng.integers(1, 8))
+            src = int(rng.integers(0, len(h) - m - 1))
+            h[-m:] = h[src:src + m]
+    offs = np.concatenate([[0], np.cumsum([len(h) for h in hists])]).astype(np.int64)
+    flat = np.array([t for h in hists for t in h] or [0], np.int32)
+    return hists, torch.tensor(flat, device=DEV), torch.tensor(offs, device=DEV)
+
+
+@pytest.mark.parametrize("lanes,max_len,vocab,k,mmin,mmax", [(200, 60, 4, 3, 1, 4), (37, 3000, 50, 8, 2, 6),
+                                                            (5, 100000, 1000, 15, 1, 16), (64, 10, 2, 1, 3, 3)])
+def test_ngram_drafts_match_the_oracle(lanes, max_len, vocab, k, mmin, mmax):
+    from oracle import ngram as ong
+    rng = np.random.default_rng(lanes * 7 + k)
+    hists, flat, offs = _ngram_case(rng, lanes, max_len, vocab)
+    drafts = torch.full((lanes, k + 2), -5, dtype=torch.int32, device=DEV)
+    lens = torch.full((lanes,), -5, dtype=torch.int32, device=DEV)
+    sv.spec_ngram_draft(flat, offs, k, drafts, lens, match_min=mmin, match_max=mmax)
+    torch.cuda.synchronize()
+    d, l = drafts.cpu().numpy(), lens.cpu().numpy()
+    found = 0
+    for b, h in enumerate(hists):
+        want = ong.ngram_draft(h, k, mmin, mmax)[0]
+        assert l[b] == len(want), (b, l[b], want)
+        assert d[b, :len(want)].tolist() == want, b
+        assert (d[b, len(want):] == -5).all()  # slots past the drafts are untouched
+        found += len(want) > 0
+    assert found > 0
+
+
+def test_ngram_argument_errors():
+    lib = sv.load_library()
+    z64 = torch.zeros(3, dtype=torch.int64, device=DEV)
+    z32 = torch.zeros(8, dtype=torch.int32, device=DEV)
+    for k, stride, mmin, mmax in [(16, 16, 1, 4), (3, 2, 1, 4), (3, 3, 0, 4), (3, 3, 3, 2), (3, 3, 1, 17)]:
+        assert lib.spec_ngram_draft(z32.data_ptr(), z64.data_ptr(), 2, k, mmin, mmax, z32.data_ptr(), stride,
+                                    z32.data_ptr(), None) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_ngram_draft(None, None, 2, 3, 1, 4, None, 3, None, None) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_ngram_draft(None, None, 0, 3, 1, 4, None, 3, None, None) == sv.SPEC_OK
