@@ -8,9 +8,10 @@ with the CUDA library (no kernels, headers, helpers or constant tables) and
 never calls it; the product path never calls this package.
 
 ``oracle.metrics`` counts the acceptance metrics of verify rounds,
-``oracle.backoff`` is the per-lane miss back-off of a drafter and
-``oracle.ngram`` the copy-from-the-conversation drafter; all are plain Python
-restatements of the pages' rules.
+``oracle.backoff`` is the per-lane miss back-off of a drafter,
+``oracle.ngram`` the copy-from-the-conversation drafter and
+``oracle.penalties`` the per-row presence / frequency penalties; all are plain
+Python restatements of the pages' rules.
 
 Every function is pinned by ``-m "not gpu"`` tests against facts fixed outside
 the oracle itself: the pages' worked examples, exact enumeration of the
@@ -18,7 +19,7 @@ acceptance rule on tiny vocabularies, a closed form, library routines (numpy's
 Philox4x64, scipy's softmax / logsumexp) and invariants.
 """
 
-from . import backoff, metrics, ngram
+from . import backoff, metrics, ngram, penalties
 from .philox import philox4x64_10, round_uniforms, word_to_uniform
 from .verify import (
     DEFAULT_ROW_BUDGET,

@@ -613,6 +613,66 @@ def check_ngram_brute_force(seed=8):
         assert got == want, (h, k, mmin, mmax, got, want)
 
 
+# ---------------------------------------------------------------------------
+# Presence / frequency penalties (FreeToken #828, PR #836), read as the usual rule
+# ---------------------------------------------------------------------------
+from oracle import penalties as opn
+
+
+def check_bf16_rounding_against_torch(seed=12):
+    """Round-to-nearest-even to bf16 equals torch's float32 -> bfloat16."""
+    import torch
+    rng = np.random.default_rng(seed)
+    x = np.concatenate([rng.normal(0, 3, 20000), rng.normal(0, 1e-3, 2000), rng.normal(0, 1e4, 2000)]).astype(np.float32)
+    # values exactly halfway between two bf16 numbers
+    half = (rng.integers(0, 1 << 15, 2000).astype(np.uint32) << 16 | 0x8000).view(np.float32)
+    x = np.concatenate([x, half[np.isfinite(half)]])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(opn.round_to_bf16(x), want)
+
+
+def check_penalty_rule_by_hand():
+    """Counts and arithmetic of the rule, worked by hand."""
+    # count 2, presence 0.5, frequency 0.25: 3 - (0.5 + 2 * 0.25) = 2
+    assert opn.penalise_value(3.0, 2, 0.5, 0.25, "bf16") == 2.0
+    # count 3, frequency only: 1 - 1.5 = -0.5
+    assert opn.penalise_value(1.0, 3, 0.0, 0.5, "f32") == -0.5
+    # no penalty leaves a bf16 logit as it is
+    assert opn.penalise_value(1.3984375, 4, 0.0, 0.0, "bf16") == 1.3984375
+    # fp32 arithmetic, then bf16 rounding: 1 - 1e-3 is 0.999 in fp32, 1.0 in bf16
+    assert opn.penalise_value(1.0, 1, 1e-3, 0.0, "f32") == float(np.float32(1.0) - np.float32(1e-3))
+    assert opn.penalise_value(1.0, 1, 1e-3, 0.0, "bf16") == 1.0
+    # row j counts the history and d_1..d_j
+    hist = {5: 1}
+    assert opn.row_counts(hist, [5, 7], 0) == {5: 1}
+    assert opn.row_counts(hist, [5, 7], 1) == {5: 2}
+    assert opn.row_counts(hist, [5, 7], 2) == {5: 2, 7: 1}
+
+
+def check_penalties_on_a_round():
+    """A lane of 3 rows: only listed tokens and earlier drafts move; a penalised
+    argmax hands the argmax to the runner-up, and the drafter's rows are left alone."""
+    V = 8
+    target = np.zeros((3, V))
+    target[:, 2] = 5.0   # the argmax of every row
+    target[:, 6] = 4.5   # the runner-up
+    drafts = np.array([2, 6, -1], np.int32)
+    out = opn.apply_penalties(target, "f32", drafts, np.array([2]), np.array([0, 3]),
+                              pen_tokens=np.array([2]), pen_counts=np.array([1]), pen_offsets=np.array([0, 1]),
+                              presence=np.array([1.0], np.float32), frequency=np.array([0.0], np.float32))
+    assert out[0, 2] == 4.0 and out[1, 2] == 4.0 and out[2, 2] == 4.0   # count 1, 2, 2: presence only
+    assert out[0, 6] == 4.5 and out[1, 6] == 4.5 and out[2, 6] == 3.5   # d_2 = 6 counts from row 2 on
+    assert np.array_equal(out[:, [0, 1, 3, 4, 5, 7]], target[:, [0, 1, 3, 4, 5, 7]])
+    res = oracle.verify_round(out, None, drafts, [2], [0, 3], np.array([0.0], np.float32))
+    assert res.out_tokens[0] == 6  # the penalised argmax gave way; d_1 = 2 is rejected
+    assert res.committed[0] == 1
+    # with frequency the counts scale
+    out = opn.apply_penalties(target, "f32", drafts, np.array([2]), np.array([0, 3]),
+                              pen_tokens=np.array([2]), pen_counts=np.array([3]), pen_offsets=np.array([0, 1]),
+                              presence=np.array([0.0], np.float32), frequency=np.array([0.5], np.float32))
+    assert out[0, 2] == 3.5 and out[1, 2] == 3.0 and out[2, 2] == 3.0
+
+
 ALL_CHECKS = [
     check_row_budget_worked_example,
     check_guess_check_table,
@@ -635,4 +695,7 @@ ALL_CHECKS = [
     check_backoff_passes_without_speculation,
     check_ngram_hand_examples,
     check_ngram_brute_force,
+    check_bf16_rounding_against_torch,
+    check_penalty_rule_by_hand,
+    check_penalties_on_a_round,
 ]

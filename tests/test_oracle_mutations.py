@@ -227,6 +227,38 @@ def test_ngram_mistakes_are_caught(monkeypatch, bad):
         oc.check_ngram_brute_force()
 
 
+import oracle.penalties as opn
+
+
+def _round_toward_zero(x32):
+    bits = np.asarray(x32, np.float32).view(np.uint32) & np.uint32(0xFFFF0000)
+    return bits.view(np.float32)
+
+
+def _row_counts_one_more(history_counts, drafts, j):
+    return _orig_row_counts(history_counts, drafts, j + 1)
+
+
+def _penalise_frequency_only(x, c, presence, frequency, dtype):
+    return _orig_penalise(x, c, 0.0, frequency, dtype)
+
+
+_orig_row_counts = opn.row_counts
+_orig_penalise = opn.penalise_value
+
+
+@pytest.mark.parametrize("name,bad,check", [
+    ("round_to_bf16", _round_toward_zero, oc.check_bf16_rounding_against_torch),
+    ("row_counts", _row_counts_one_more, oc.check_penalty_rule_by_hand),
+    ("row_counts", _row_counts_one_more, oc.check_penalties_on_a_round),
+    ("penalise_value", _penalise_frequency_only, oc.check_penalty_rule_by_hand),
+])
+def test_penalty_mistakes_are_caught(monkeypatch, name, bad, check):
+    monkeypatch.setattr(opn, name, bad)
+    with pytest.raises(AssertionError):
+        check()
+
+
 def test_philox_round_count_matters(monkeypatch):
     import oracle.philox as ph
     monkeypatch.setattr(ph, "ROUNDS", 9)
