@@ -521,6 +521,35 @@ def round_control_timing(device, stream, reps=500):
         torch.cuda.synchronize()
         entry["ngram_draft_us"] = e0.elapsed_time(e1) * 1e3 / reps
         entry["ngram_history_tokens"] = hist
+        # per-row penalties: 8 rows a lane, 200 penalised history tokens a lane
+        V = 151936 if lanes <= 128 else 8192
+        kk = torch.full((lanes,), 7, dtype=torch.int32, device=device)
+        offs_r = (torch.arange(lanes + 1, dtype=torch.int32) * 8).to(device)
+        logits = torch.zeros(lanes * 8, V, dtype=torch.bfloat16, device=device)
+        dtok = torch.randint(0, V, (lanes * 8,), generator=g, dtype=torch.int32).to(device)
+        ptok = torch.sort(torch.randperm(V, generator=g)[:200].to(torch.int32)).values.repeat(lanes).to(device)
+        pcnt = torch.ones(lanes * 200, dtype=torch.int32, device=device)
+        poff = (torch.arange(lanes + 1, dtype=torch.int64) * 200).to(device)
+        pres = torch.full((lanes,), 0.5, dtype=torch.float32, device=device)
+        fn = lambda: sv.spec_apply_penalties(logits, offs_r, dtok, kk, ptok, pcnt, poff, pres, pres, stream=stream)
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(reps):
+                    fn()
+        graph.replay()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        entry["penalties_us"] = e0.elapsed_time(e1) * 1e3 / reps
+        entry["penalties_shape"] = {"rows_per_lane": 8, "history_tokens": 200, "vocab": V}
+        del logits
         entry["bound"] = ("launch latency at 128 lanes; the drafter reads 4 B per history token once (repeats hit L1),"
                           " so large batches are bound by memory latency")
         out[f"lanes_{lanes}"] = entry

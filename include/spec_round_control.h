@@ -1,7 +1,7 @@
 /*
  * spec_round_control.h -- the rest of a speculative round around the verify:
- * acceptance metrics, the per-lane miss back-off of a drafter, and the
- * copy-from-the-conversation (n-gram) drafter.
+ * acceptance metrics, the per-lane miss back-off of a drafter, the
+ * copy-from-the-conversation (n-gram) drafter and per-row logit penalties.
  *
  * The first two consume the per-lane outputs of spec_verify_accept (committed
  * counts, the draft lengths the round used, lane_status), the drafter writes
@@ -145,6 +145,37 @@ int spec_backoff_step(spec_backoff_state* states, const int32_t* proposed, const
 int spec_ngram_draft(const int32_t* tokens, const int64_t* hist_offsets, int32_t lanes, int32_t k,
                      int32_t match_min, int32_t match_max, int32_t* drafts, int32_t draft_stride,
                      int32_t* draft_lens, void* stream);
+
+/*
+ * spec_apply_penalties -- per-row presence and frequency penalties on the
+ * target logits of a round (FreeToken tracking issue #828, "PRs": #836 verifies
+ * on the target side with per-row presence and frequency penalties), applied
+ * in place, on the same stream, right before spec_verify_accept.
+ *
+ * Row j of lane b scores the position after the anchor and d_1..d_j, so token
+ * t's count in that row is c = (its count in the lane's history) + (its count
+ * among d_1..d_j).  Every token with c > 0 gets
+ *     z = x - (frequency[b] * c + presence[b])
+ * in fp32 with the roundings in that order (product, sum, difference); a bf16
+ * logit is then rounded to the nearest bf16 (ties to even) and stored back.
+ * Other tokens, the drafter's logits and lanes whose row_offsets disagree with
+ * draft_lens (spec_verify_accept reports those) are not touched.
+ *
+ * target_logits, dtype, ld, V, lanes, row_offsets, draft_tokens and
+ * draft_lens are those of the round's spec_verify_args.  Lane b's history
+ * counts are pen_tokens / pen_counts [pen_offsets[b] .. pen_offsets[b + 1]):
+ * distinct token ids in ascending order with counts >= 1; ids outside [0, V)
+ * are ignored.  presence and frequency are per lane (may be NULL: 0).  One CTA
+ * per lane; touches (history + drafts) x (k_b + 1) logits of the lane.
+ *
+ * Errors: SPEC_ERR_INVALID_ARG for NULL target_logits / row_offsets /
+ * draft_tokens / draft_lens / pen_* with lanes > 0, lanes < 0, V <= 0, ld < V
+ * or an unknown dtype; SPEC_ERR_CUDA if the launch fails.
+ */
+int spec_apply_penalties(void* target_logits, spec_dtype dtype, int64_t ld, int32_t V, int32_t lanes,
+                         const int32_t* row_offsets, const int32_t* draft_tokens, const int32_t* draft_lens,
+                         const int32_t* pen_tokens, const int32_t* pen_counts, const int64_t* pen_offsets,
+                         const float* presence, const float* frequency, void* stream);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,7 @@ __all__ = [
     "spec_verify_launch_shape", "spec_round_uniforms", "new_row_stats", "row_stats_view",
     "spec_accept_counts_update", "spec_accept_rates_from_counts", "new_accept_counts", "accept_counts_view",
     "spec_backoff_step", "new_backoff_states", "BACKOFF_FIELDS", "ACCEPT_COUNT_WORDS",
-    "spec_ngram_draft", "SPEC_NGRAM_MAX_MATCH",
+    "spec_ngram_draft", "SPEC_NGRAM_MAX_MATCH", "spec_apply_penalties",
 ]
 
 SPEC_OK = 0
@@ -126,6 +126,9 @@ def load_library():
     lib.spec_ngram_draft.restype = ctypes.c_int
     lib.spec_ngram_draft.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                      ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    lib.spec_apply_penalties.restype = ctypes.c_int
+    lib.spec_apply_penalties.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32] + \
+        [ctypes.c_void_p] * 9
     lib.spec_backoff_step.restype = ctypes.c_int
     lib.spec_backoff_step.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
@@ -415,3 +418,32 @@ def spec_ngram_draft(tokens, hist_offsets, k, drafts, draft_lens, match_min=1, m
                               _ptr(drafts), drafts.stride(0), _ptr(draft_lens), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_ngram_draft")
+
+
+def spec_apply_penalties(target, row_offsets, draft_tokens, draft_lens, pen_tokens, pen_counts, pen_offsets,
+                         presence=None, frequency=None, stream=None):
+    """Per-row presence / frequency penalties on the target logits, in place
+    (see spec_apply_penalties in include/spec_round_control.h).  target: the
+    round's [rows, >= V] bf16/float32 logits (V = target.shape[1], ld its row
+    stride); pen_tokens / pen_counts int32 [n] (per lane ascending distinct ids),
+    pen_offsets int64 [lanes + 1]; presence / frequency float32 [lanes] or None."""
+    lib = load_library()
+    if target.dim() != 2 or target.stride(1) != 1 or target.dtype not in _DTYPES:
+        raise ValueError("target must be a 2-D bf16/float32 tensor with unit inner stride")
+    dev = target.device
+    lanes = draft_lens.numel()
+    _need(row_offsets, "row_offsets", torch.int32, dev, lanes + 1)
+    _need(draft_tokens, "draft_tokens", torch.int32, dev)
+    _need(draft_lens, "draft_lens", torch.int32, dev)
+    _need(pen_tokens, "pen_tokens", torch.int32, dev)
+    _need(pen_counts, "pen_counts", torch.int32, dev, pen_tokens.numel())
+    _need(pen_offsets, "pen_offsets", torch.int64, dev, lanes + 1)
+    for t, name in ((presence, "presence"), (frequency, "frequency")):
+        if t is not None:
+            _need(t, name, torch.float32, dev, lanes)
+    rc = lib.spec_apply_penalties(_ptr(target), _DTYPES[target.dtype], target.stride(0), target.shape[1], lanes,
+                                  _ptr(row_offsets), _ptr(draft_tokens), _ptr(draft_lens), _ptr(pen_tokens),
+                                  _ptr(pen_counts), _ptr(pen_offsets), _ptr(presence), _ptr(frequency),
+                                  _stream(stream))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_apply_penalties")

@@ -1,6 +1,8 @@
-// round_control.cu -- acceptance counts, the per-lane miss back-off and the
-// copy-from-the-conversation drafter: the C ABI of include/spec_round_control.h.
+// round_control.cu -- acceptance counts, the per-lane miss back-off, the
+// copy-from-the-conversation drafter and per-row logit penalties: the C ABI of
+// include/spec_round_control.h.
 // All run on the device next to the verify kernel; none allocates memory.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -167,6 +169,82 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_draft_kernel(const int32_
   if (threadIdx.x == 0) draft_lens[b] = n;
 }
 
+// Per-row presence / frequency penalties (FreeToken #828, PR #836), one CTA
+// per lane.  Row j's count of a token is its history count plus its count
+// among d_1..d_j.  Each thread rewrites whole tokens of one row: first the
+// listed history tokens, then the first occurrence of each draft d_1..d_j that
+// is not in the (sorted) history list, so every logit is written at most once.
+template <bool BF16>
+__global__ void __launch_bounds__(256) apply_penalties_kernel(uint8_t* target, int64_t ld_bytes, int32_t V,
+                                                              const int32_t* row_offsets,
+                                                              const int32_t* draft_tokens,
+                                                              const int32_t* draft_lens, const int32_t* pen_tokens,
+                                                              const int32_t* pen_counts,
+                                                              const int64_t* pen_offsets, const float* presence,
+                                                              const float* frequency) {
+  const int b = blockIdx.x;
+  const int k = draft_lens[b];
+  const int off = row_offsets[b];
+  if (k < 0 || k > SPEC_MAX_DRAFTS || row_offsets[b + 1] - off != k + 1) return;
+  const int64_t h0 = pen_offsets[b], h1 = pen_offsets[b + 1];
+  const float pres = presence ? presence[b] : 0.f;
+  const float freq = frequency ? frequency[b] : 0.f;
+  int d[SPEC_MAX_DRAFTS];
+#pragma unroll
+  for (int i = 0; i < SPEC_MAX_DRAFTS; ++i) d[i] = (i < k) ? draft_tokens[off + i] : -1;
+
+  auto penalise = [&](int row, int t, int c) {
+    uint8_t* r = target + static_cast<int64_t>(off + row) * ld_bytes;
+    const float m = __fmul_rn(freq, static_cast<float>(c));
+    const float delta = __fadd_rn(m, pres);
+    if constexpr (BF16) {
+      __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(r) + t;
+      *p = __float2bfloat16_rn(__fsub_rn(__bfloat162float(*p), delta));
+    } else {
+      float* p = reinterpret_cast<float*>(r) + t;
+      *p = __fsub_rn(*p, delta);
+    }
+  };
+  auto in_history = [&](int t) {  // binary search of the sorted list
+    int64_t lo = h0, hi = h1;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      const int v = pen_tokens[mid];
+      if (v == t) return true;
+      if (v < t) lo = mid + 1;
+      else hi = mid;
+    }
+    return false;
+  };
+
+  const int64_t nh = h1 > h0 ? h1 - h0 : 0;
+  for (int j = 0; j <= k; ++j) {
+    // history tokens of row j
+    for (int64_t e = threadIdx.x; e < nh; e += blockDim.x) {
+      const int t = pen_tokens[h0 + e];
+      if (t < 0 || t >= V) continue;
+      int c = pen_counts[h0 + e];
+#pragma unroll
+      for (int i = 0; i < SPEC_MAX_DRAFTS; ++i) c += (i < j && d[i] == t) ? 1 : 0;
+      if (c > 0) penalise(j, t, c);
+    }
+    // drafts of row j that the history does not list (first occurrence only)
+    if (threadIdx.x < j) {
+      const int i = threadIdx.x;
+      const int t = d[i];
+      bool first = (t >= 0 && t < V);
+      int c = 0;
+      for (int q = 0; q < j; ++q) {
+        if (d[q] == t) {
+          ++c;
+          if (q < i) first = false;
+        }
+      }
+      if (first && !in_history(t)) penalise(j, t, c);
+    }
+  }
+}
+
 int launch_status() { return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
 
 // (1 - alpha^(g + 1)) / (1 - alpha): expected tokens a round of independent
@@ -260,6 +338,27 @@ int spec_ngram_draft(const int32_t* tokens, const int64_t* hist_offsets, int32_t
     return SPEC_ERR_INVALID_ARG;
   ngram_draft_kernel<<<lanes, kNgramThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       tokens, hist_offsets, k, match_min, match_max, drafts, draft_stride, draft_lens);
+  return launch_status();
+}
+
+int spec_apply_penalties(void* target_logits, spec_dtype dtype, int64_t ld, int32_t V, int32_t lanes,
+                         const int32_t* row_offsets, const int32_t* draft_tokens, const int32_t* draft_lens,
+                         const int32_t* pen_tokens, const int32_t* pen_counts, const int64_t* pen_offsets,
+                         const float* presence, const float* frequency, void* stream) {
+  if (lanes < 0 || V <= 0 || ld < V || (dtype != SPEC_F32 && dtype != SPEC_BF16)) return SPEC_ERR_INVALID_ARG;
+  if (lanes == 0) return SPEC_OK;
+  if (target_logits == nullptr || row_offsets == nullptr || draft_tokens == nullptr || draft_lens == nullptr ||
+      pen_tokens == nullptr || pen_counts == nullptr || pen_offsets == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* t = static_cast<uint8_t*>(target_logits);
+  if (dtype == SPEC_BF16) {
+    apply_penalties_kernel<true><<<lanes, 256, 0, st>>>(t, ld * 2, V, row_offsets, draft_tokens, draft_lens,
+                                                        pen_tokens, pen_counts, pen_offsets, presence, frequency);
+  } else {
+    apply_penalties_kernel<false><<<lanes, 256, 0, st>>>(t, ld * 4, V, row_offsets, draft_tokens, draft_lens,
+                                                         pen_tokens, pen_counts, pen_offsets, presence, frequency);
+  }
   return launch_status();
 }
 

@@ -184,3 +184,67 @@ def test_ngram_argument_errors():
                                     z32.data_ptr(), None) == sv.SPEC_ERR_INVALID_ARG
     assert lib.spec_ngram_draft(None, None, 2, 3, 1, 4, None, 3, None, None) == sv.SPEC_ERR_INVALID_ARG
     assert lib.spec_ngram_draft(None, None, 0, 3, 1, 4, None, 3, None, None) == sv.SPEC_OK
+
+
+# ---------------------------------------------------------------------------
+# per-row presence / frequency penalties
+# ---------------------------------------------------------------------------
+def _penalty_lists(rng, r, max_hist):
+    V = r.vocab
+    toks, counts, offs = [], [], [0]
+    dt = r.draft_tokens.cpu().numpy()
+    off = r.row_offsets.cpu().numpy()
+    for b in range(r.lanes):
+        n = int(rng.integers(0, max_hist + 1))
+        pool = set(int(x) for x in rng.integers(0, V, n))
+        # some drafts of the lane are in the history too, and the row argmaxes
+        for j in range(int(off[b + 1] - off[b]) - 1):
+            if rng.random() < 0.5:
+                pool.add(int(dt[off[b] + j]))
+        pool.add(int(r.target[off[b]].float().argmax()))
+        t = sorted(pool)
+        toks += t
+        counts += [int(c) for c in rng.integers(1, 4, len(t))]
+        offs.append(len(toks))
+    to = lambda a, d: torch.tensor(np.asarray(a), dtype=d, device=DEV)
+    return to(toks or [0], torch.int32), to(counts or [1], torch.int32), to(offs, torch.int64)
+
+
+@pytest.mark.parametrize("dtype,sampled,seed", [("bf16", "mixed", 1), ("f32", "mixed", 2), ("bf16", "none", 3),
+                                                ("bf16", "all", 4)])
+def test_penalties_match_the_oracle_and_feed_the_verify(dtype, sampled, seed):
+    from gpu_harness import compare, logits_to_numpy, run_oracle
+    from oracle import penalties as opn
+    rng = np.random.default_rng(seed)
+    r = workloads.make_custom_round(600 + seed, DEV, lanes=19, vocab=30011, kmax=7, dtype=dtype, sampled=sampled)
+    # repeated drafts within a lane
+    dt = r.draft_tokens.clone()
+    off = r.row_offsets.cpu().numpy()
+    for b in range(0, r.lanes, 3):
+        if off[b + 1] - off[b] > 2:
+            dt[off[b] + 1] = dt[off[b]]
+    r.draft_tokens = dt
+    toks, counts, offs = _penalty_lists(rng, r, 200)
+    pres = torch.tensor(rng.uniform(0, 2, r.lanes), dtype=torch.float32, device=DEV)
+    freq = torch.tensor(rng.uniform(0, 1, r.lanes), dtype=torch.float32, device=DEV)
+    pres[0], freq[0] = 0.0, 0.0
+    before = logits_to_numpy(r.target, r.vocab)
+    sv.spec_apply_penalties(r.target, r.row_offsets, r.draft_tokens, r.draft_lens, toks, counts, offs, pres, freq)
+    torch.cuda.synchronize()
+    got = logits_to_numpy(r.target, r.vocab)
+    want = opn.apply_penalties(before, dtype, r.draft_tokens.cpu().numpy(), r.draft_lens.cpu().numpy(), off,
+                               toks.cpu().numpy(), counts.cpu().numpy(), offs.cpu().numpy(),
+                               pres.cpu().numpy(), freq.cpu().numpy())
+    np.testing.assert_array_equal(got, want)
+    assert (got != before).sum() > r.lanes
+    # the verify on the penalised logits against the oracle's verify on its own penalised copy
+    compare(r, run_gpu(r), run_oracle(r))
+
+
+def test_penalties_argument_errors():
+    lib = sv.load_library()
+    assert lib.spec_apply_penalties(None, 1, 10, 10, -1, *([None] * 9)) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_apply_penalties(None, 1, 10, 10, 2, *([None] * 9)) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_apply_penalties(None, 1, 9, 10, 0, *([None] * 9)) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_apply_penalties(None, 7, 10, 10, 0, *([None] * 9)) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_apply_penalties(None, 1, 10, 10, 0, *([None] * 9)) == sv.SPEC_OK
