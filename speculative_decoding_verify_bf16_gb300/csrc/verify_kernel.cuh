@@ -792,11 +792,14 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   int b = blockIdx.x / C;
 
   // ---- set-up that touches only shared memory (overlaps the previous kernel) ----
-  if (tid == 0) {
-    for (int s = 0; s < p.nslots - p.nslots % kGroups; ++s) {
-      mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], kPieces);
-    }
+  // One thread per ring slot initialises its pair of barriers (another thread
+  // the exchange barriers); each makes its initialisations visible to the
+  // cluster's async proxy before the barrier that follows.
+  if (tid < p.nslots - p.nslots % kGroups) {
+    mbar_init(&sh.full[tid], 1);
+    mbar_init(&sh.empty[tid], kPieces);
+    fence_mbar_init();
+  } else if (tid == 32 + kMaxSlots) {
     mbar_init(&sh.xbar, 1);
     mbar_init(&sh.dbar[0], 1);
     mbar_init(&sh.dbar[1], 1);
