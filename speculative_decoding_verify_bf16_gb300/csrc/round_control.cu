@@ -171,9 +171,10 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_draft_kernel(const int32_
 
 // Per-row presence / frequency penalties (FreeToken #828, PR #836), one CTA
 // per lane.  Row j's count of a token is its history count plus its count
-// among d_1..d_j.  Each thread rewrites whole tokens of one row: first the
-// listed history tokens, then the first occurrence of each draft d_1..d_j that
-// is not in the (sorted) history list, so every logit is written at most once.
+// among d_1..d_j.  Threads take (row, history entry) pairs of all the lane's
+// rows at once, and (row, draft) pairs for the first occurrence of each draft
+// d_1..d_j that is not in the (sorted) history list, so every logit is read and
+// written by one thread, once.
 template <bool BF16>
 __global__ void __launch_bounds__(256) apply_penalties_kernel(uint8_t* target, int64_t ld_bytes, int32_t V,
                                                               const int32_t* row_offsets,
@@ -218,19 +219,23 @@ __global__ void __launch_bounds__(256) apply_penalties_kernel(uint8_t* target, i
   };
 
   const int64_t nh = h1 > h0 ? h1 - h0 : 0;
-  for (int j = 0; j <= k; ++j) {
-    // history tokens of row j
-    for (int64_t e = threadIdx.x; e < nh; e += blockDim.x) {
-      const int t = pen_tokens[h0 + e];
-      if (t < 0 || t >= V) continue;
-      int c = pen_counts[h0 + e];
+  // (row, history entry) pairs, all rows at once
+  for (int64_t idx = threadIdx.x; idx < (k + 1) * nh; idx += blockDim.x) {
+    const int j = static_cast<int>(idx / nh);
+    const int64_t e = idx - j * nh;
+    const int t = pen_tokens[h0 + e];
+    if (t < 0 || t >= V) continue;
+    int c = pen_counts[h0 + e];
 #pragma unroll
-      for (int i = 0; i < SPEC_MAX_DRAFTS; ++i) c += (i < j && d[i] == t) ? 1 : 0;
-      if (c > 0) penalise(j, t, c);
-    }
-    // drafts of row j that the history does not list (first occurrence only)
-    if (threadIdx.x < j) {
-      const int i = threadIdx.x;
+    for (int i = 0; i < SPEC_MAX_DRAFTS; ++i) c += (i < j && d[i] == t) ? 1 : 0;
+    if (c > 0) penalise(j, t, c);
+  }
+  // (row j, draft i < j) pairs for drafts the history does not list, first
+  // occurrence of each token in d_1..d_j only
+  static_assert((SPEC_MAX_DRAFTS + 1) * (SPEC_MAX_DRAFTS + 1) <= 256, "one thread per (row, draft) pair");
+  {
+    const int j = threadIdx.x / (SPEC_MAX_DRAFTS + 1), i = threadIdx.x % (SPEC_MAX_DRAFTS + 1);
+    if (j <= k && i < j) {
       const int t = d[i];
       bool first = (t >= 0 && t < V);
       int c = 0;
