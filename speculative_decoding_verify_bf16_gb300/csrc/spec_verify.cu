@@ -70,7 +70,7 @@ struct VerifyShape {
 // CTA's share of an average lane (rows / lanes rows, counted 1.5 times for
 // drafter rows of sampled lanes) at or below 1 MB; never fewer than 2048
 // elements per CTA.  The caller then shrinks it until clusters fit (see
-// spec_verify_accept).  The ring holds whole slices when they fit a 32 KB slot.
+// spec_verify_accept).  The ring holds whole slices when they fit a 40 KB slot.
 VerifyShape choose_shape(int lanes, int rows, int V, int esize, bool aligned, int sms, int smem_optin,
                          int force_cluster) {
   VerifyShape s{};
@@ -96,7 +96,9 @@ VerifyShape choose_shape(int lanes, int rows, int V, int esize, bool aligned, in
     return s;
   }
   const int64_t slice_bytes = static_cast<int64_t>(s.slice) * esize;
-  const int64_t slot_max = static_cast<int64_t>(env_int("SPEC_VERIFY_SLOT_KB", 32)) * 1024;
+  // Slots of up to 40 KB: a 152 KB slice then streams in four 38 KB pieces,
+  // one per consumer-warp group (measured faster than five of 30 KB).
+  const int64_t slot_max = static_cast<int64_t>(env_int("SPEC_VERIFY_SLOT_KB", 40)) * 1024;
   const int64_t chunks = (slice_bytes + slot_max - 1) / slot_max;
   s.slot_bytes = static_cast<int>(round_up((slice_bytes + chunks - 1) / chunks, 16));
   // With 8 consumer warps 88 KB keeps two CTAs per SM possible; with 16 the
