@@ -199,10 +199,11 @@ class Bench:
                 out_tokens=torch.zeros(s.rows, dtype=torch.int32, device=device),
                 status=torch.zeros(s.lanes, dtype=torch.int32, device=device)))
         # Ranks verify disjoint lane ranges of one notional batch: lane_base keys
-        # their uniforms by global lane index.
+        # their uniforms by global lane index.  Every set's metadata is written
+        # once, before the timed launches, so no kernel on the stream writes it.
         self.args = [sv.make_args(s.target, s.draft, s.draft_tokens, s.draft_lens, s.row_offsets,
                                   s.temperatures, s.seed, o["committed"], o["out_tokens"], o["status"],
-                                  rows=s.rows, lane_base=rank * s.lanes)
+                                  rows=s.rows, lane_base=rank * s.lanes, meta_before_wait=True)
                      for s, o in zip(self.sets, self.outs)]
         self.verify_bytes, self.rows_per_step = round_bytes(first)
         self.has_state = first.staged is not None
@@ -325,8 +326,9 @@ def e2e_run(bench, steps, stream):
         stream.wait_event(uploaded[i % 2])
         dt, dl, ro, te = views(d)
         r = res_dev[i % 2]
+        # the metadata comes from the copy stream (behind the event), not from a kernel
         sv.spec_verify_accept(d["target"], d.get("draft"), dt, dl, ro, te, s0.seed + i, r[:lanes], r[lanes:],
-                              stream=stream)
+                              stream=stream, meta_before_wait=True)
         consumed[i % 2].record(stream)
         res_host[i % 2].copy_(r, non_blocking=True)
 

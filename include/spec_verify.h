@@ -56,6 +56,19 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 #define SPEC_MAX_DRAFTS 15
 
 /*
+ * Flags of spec_verify_args.flags.
+ *
+ * SPEC_VERIFY_META_BEFORE_WAIT: draft_tokens, draft_lens, row_offsets and
+ * temperatures were written before the kernel that precedes this launch on
+ * the stream began (by an earlier kernel, a copy or the host).  The kernel then
+ * reads them while it waits for that kernel to finish (programmatic dependent
+ * launch), which takes one global-memory round trip off each launch.  Without
+ * the flag it reads them after the wait, as it must when the preceding kernel
+ * produces them.  The logits are always read after the wait.
+ */
+#define SPEC_VERIFY_META_BEFORE_WAIT 1u
+
+/*
  * spec_row_budget -- drafts per lane under a row budget.
  *
  * ignis docs, "Speculative decoding" -- "The row budget": a round carries
@@ -114,6 +127,7 @@ typedef struct {
                                    split into parts (GPUs, streams) with lane_base = the
                                    part's first global lane draws exactly the uniforms
                                    of the unsplit batch; 0 otherwise                */
+  uint32_t flags;               /* SPEC_VERIFY_* flags above; 0 for none          */
 } spec_verify_args;
 
 /*
@@ -134,6 +148,12 @@ typedef struct {
  * al., SC'11) with key (seed, 0) and counter (j, lane_base + b, 0, 0): word 0 gives u_j,
  * word 1 gives the draw's u'; u = (word >> 40) * 2^-24.  The draw walks token ids
  * upwards and takes the first whose cumulative weight exceeds u' * W.
+ *
+ * Launch: one thread-block cluster per lane.  A round with draft_logits runs
+ * a build of the kernel with 20 consumer warps per CTA (its sampled lanes are
+ * bound by instruction issue), a round without them the 16-warp build; both
+ * compute the same results.  The environment variable SPEC_VERIFY_WARPS=16 or
+ * 20 forces one build.
  *
  * Errors: returns SPEC_ERR_INVALID_ARG for NULL required pointers, V <= 0,
  * lanes <= 0, rows < lanes, ld < V or an unknown dtype; SPEC_ERR_CUDA if the
@@ -200,11 +220,14 @@ const char* spec_status_string(int status);
  * memory per CTA, for a verify over `lanes` lanes and `rows` rows of vocabulary
  * V in `dtype` with 16-byte aligned rows on the current device, after the
  * cluster has been shrunk to what the device can schedule (the same rule the
- * launch applies).  Any output pointer may be NULL.  Returns SPEC_OK,
- * SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED or SPEC_ERR_CUDA.
+ * launch applies).  `with_draft` != 0 asks for the launch of a round that
+ * passes drafter logits: such rounds run a build of the kernel with more
+ * consumer warps per CTA (see spec_verify_accept).  Any output pointer may be
+ * NULL.  Returns SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED or
+ * SPEC_ERR_CUDA.
  */
-int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype dtype, int32_t* cluster_ctas,
-                             int32_t* threads, int32_t* slice, int32_t* smem_bytes);
+int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype dtype, int32_t with_draft,
+                             int32_t* cluster_ctas, int32_t* threads, int32_t* slice, int32_t* smem_bytes);
 
 #ifdef __cplusplus
 }

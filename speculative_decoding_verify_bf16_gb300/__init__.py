@@ -22,7 +22,7 @@ __all__ = [
     "spec_verify_launch_shape", "spec_round_uniforms", "new_row_stats", "row_stats_view",
     "spec_accept_counts_update", "spec_accept_rates_from_counts", "new_accept_counts", "accept_counts_view",
     "spec_backoff_step", "new_backoff_states", "BACKOFF_FIELDS", "ACCEPT_COUNT_WORDS",
-    "spec_ngram_draft", "SPEC_NGRAM_MAX_MATCH", "spec_apply_penalties",
+    "spec_ngram_draft", "SPEC_NGRAM_MAX_MATCH", "spec_apply_penalties", "SPEC_VERIFY_META_BEFORE_WAIT",
 ]
 
 SPEC_OK = 0
@@ -34,6 +34,7 @@ SPEC_ERR_TOKEN_RANGE = 5
 SPEC_ERR_LAYOUT = 6
 SPEC_ERR_TIMEOUT = 7
 SPEC_MAX_DRAFTS = 15
+SPEC_VERIFY_META_BEFORE_WAIT = 1
 
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
@@ -69,6 +70,7 @@ class _Args(ctypes.Structure):
         ("lane_status", ctypes.c_void_p),
         ("row_stats", ctypes.c_void_p),
         ("lane_base", ctypes.c_uint32),
+        ("flags", ctypes.c_uint32),
     ]
 
 
@@ -114,8 +116,8 @@ def load_library():
     lib.spec_round_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_void_p, ctypes.c_void_p]
     lib.spec_verify_launch_shape.restype = ctypes.c_int
-    lib.spec_verify_launch_shape.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int] + \
-        [ctypes.POINTER(ctypes.c_int32)] * 4
+    lib.spec_verify_launch_shape.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
+                                             ctypes.c_int32] + [ctypes.POINTER(ctypes.c_int32)] * 4
     lib.spec_accept_counts_update.restype = ctypes.c_int
     lib.spec_accept_counts_update.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                               ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
@@ -184,7 +186,7 @@ def row_stats_view(buf):
 
 def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, temperatures, seed,
                        committed, out_tokens, lane_status=None, row_stats=None, stream=None,
-                       rows=None, lane_base=0):
+                       rows=None, lane_base=0, meta_before_wait=False):
     """Launch the fused verify kernel (see spec_verify_accept in include/spec_verify.h).
 
     target, draft: [rows, >= V] bf16 or float32 CUDA tensors with unit inner
@@ -195,6 +197,9 @@ def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, tem
     ``rows`` defaults to target.shape[0] (it must equal row_offsets[-1]).
     ``lane_base`` is the global index of lane 0 in the Philox counter (a batch
     split into parts draws the uniforms of the unsplit batch).
+    ``meta_before_wait`` sets SPEC_VERIFY_META_BEFORE_WAIT: the caller promises
+    that the kernel preceding this launch on the stream did not write
+    draft_tokens, draft_lens, row_offsets or temperatures.
     """
     lib = load_library()
     if target.dim() != 2 or target.stride(1) != 1 or target.dtype not in _DTYPES:
@@ -237,6 +242,7 @@ def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, tem
         lane_status=None if lane_status is None else lane_status.data_ptr(),
         row_stats=None if row_stats is None else row_stats.data_ptr(),
         lane_base=int(lane_base),
+        flags=SPEC_VERIFY_META_BEFORE_WAIT if meta_before_wait else 0,
     )
     code = lib.spec_verify_accept(ctypes.byref(a), _stream(stream))
     if code != SPEC_OK:
@@ -249,7 +255,8 @@ def spec_verify_accept_raw(args, stream):
 
 
 def make_args(target, draft, draft_tokens, draft_lens, row_offsets, temperatures, seed,
-              committed, out_tokens, lane_status=None, row_stats=None, V=None, rows=None, lane_base=0):
+              committed, out_tokens, lane_status=None, row_stats=None, V=None, rows=None, lane_base=0,
+              meta_before_wait=False):
     """Build the C argument struct once (for tight loops that call it repeatedly)."""
     return _Args(
         target_logits=target.data_ptr(),
@@ -269,6 +276,7 @@ def make_args(target, draft, draft_tokens, draft_lens, row_offsets, temperatures
         lane_status=None if lane_status is None else lane_status.data_ptr(),
         row_stats=None if row_stats is None else row_stats.data_ptr(),
         lane_base=int(lane_base),
+        flags=SPEC_VERIFY_META_BEFORE_WAIT if meta_before_wait else 0,
     )
 
 
@@ -312,11 +320,11 @@ def spec_round_uniforms(seed, lanes, positions, lane_base=0, device=None, stream
     return out
 
 
-def spec_verify_launch_shape(lanes, rows, V, dtype=torch.bfloat16):
+def spec_verify_launch_shape(lanes, rows, V, dtype=torch.bfloat16, with_draft=False):
     """Launch shape spec_verify_accept would pick (see include/spec_verify.h)."""
     lib = load_library()
     vals = [ctypes.c_int32() for _ in range(4)]
-    code = lib.spec_verify_launch_shape(int(lanes), int(rows), int(V), _DTYPES[dtype],
+    code = lib.spec_verify_launch_shape(int(lanes), int(rows), int(V), _DTYPES[dtype], int(bool(with_draft)),
                                         *[ctypes.byref(v) for v in vals])
     if code != SPEC_OK:
         raise SpecError(code, "spec_verify_launch_shape")

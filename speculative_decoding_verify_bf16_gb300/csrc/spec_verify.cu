@@ -11,10 +11,13 @@
 #include "commit_kernel.cuh"
 #include "spec_verify.h"
 #include "verify_kernel.cuh"
+#include "verify_variants.h"
 
 namespace {
 
 using specv::bf16_tag;
+using verify_variants::KernelVariant;
+using verify_variants::w20_variant;
 
 constexpr int kMaxDevices = 64;
 
@@ -22,7 +25,7 @@ struct DeviceCache {
   bool ready = false;
   int sms = 0;
   int smem_optin = 0;
-  bool verify_attr[4] = {false, false, false, false};  // per kernel instantiation
+  bool verify_attr[8] = {};  // per kernel build and instantiation
   bool commit_attr = false;
 };
 
@@ -71,8 +74,8 @@ struct VerifyShape {
 // drafter rows of sampled lanes) at or below 1 MB; never fewer than 2048
 // elements per CTA.  The caller then shrinks it until clusters fit (see
 // spec_verify_accept).  The ring holds whole slices when they fit a 40 KB slot.
-VerifyShape choose_shape(int lanes, int rows, int V, int esize, bool aligned, int sms, int smem_optin,
-                         int force_cluster) {
+VerifyShape choose_shape(const KernelVariant& kv, int lanes, int rows, int V, int esize, bool aligned, int sms,
+                         int smem_optin, int force_cluster) {
   VerifyShape s{};
   const int vec = 16 / esize;
   int C = force_cluster > 0 ? force_cluster : env_int("SPEC_VERIFY_CLUSTER", 0);
@@ -88,7 +91,7 @@ VerifyShape choose_shape(int lanes, int rows, int V, int esize, bool aligned, in
   if (C > specv::kMaxCluster) C = specv::kMaxCluster;
   s.cluster = C;
   s.slice = static_cast<int>(round_up((V + C - 1) / C, vec));
-  s.head_bytes = static_cast<int>(round_up(sizeof(specv::SmemHead), 128));
+  s.head_bytes = static_cast<int>(round_up(kv.head_bytes_raw, 128));
   if (!aligned) {
     s.slot_bytes = 16;
     s.nslots = 0;
@@ -101,32 +104,51 @@ VerifyShape choose_shape(int lanes, int rows, int V, int esize, bool aligned, in
   const int64_t slot_max = static_cast<int64_t>(env_int("SPEC_VERIFY_SLOT_KB", 40)) * 1024;
   const int64_t chunks = (slice_bytes + slot_max - 1) / slot_max;
   s.slot_bytes = static_cast<int>(round_up((slice_bytes + chunks - 1) / chunks, 16));
-  // With 8 consumer warps 88 KB keeps two CTAs per SM possible; with 16 the
+  // With 8 consumer warps 88 KB keeps two CTAs per SM possible; with more the
   // CTA fills an SM and the ring takes all the shared memory left.
   const int64_t ring_kb = env_int("SPEC_VERIFY_RING_KB", 0);
   const int64_t ring = ring_kb > 0 ? ring_kb * 1024
-                                   : (specv::kConsumerWarps <= 8 ? 88 * 1024 : smem_optin - s.head_bytes);
+                                   : (kv.consumer_warps <= 8 ? 88 * 1024 : smem_optin - s.head_bytes);
   // A multiple of the kernel's consumer-warp groups (each group owns its slots).
   int nslots = static_cast<int>(ring / s.slot_bytes);
-  nslots -= nslots % specv::kGroups;
-  if (nslots < specv::kGroups) nslots = specv::kGroups;
-  if (nslots > specv::kMaxSlots) nslots = specv::kMaxSlots - specv::kMaxSlots % specv::kGroups;
+  nslots -= nslots % kv.groups;
+  if (nslots < kv.groups) nslots = kv.groups;
+  if (nslots > specv::kMaxSlots) nslots = specv::kMaxSlots - specv::kMaxSlots % kv.groups;
   s.nslots = nslots;
   s.smem = s.head_bytes + nslots * s.slot_bytes;
   return s;
 }
 
-template <typename T, bool ALIGNED>
-void* verify_kernel_ptr() {
-  return reinterpret_cast<void*>(&specv::verify_accept_kernel<T, ALIGNED>);
+// The 16-consumer-warp build of the kernel (this translation unit).
+KernelVariant w16_variant() {
+  KernelVariant v;
+  v.threads = specv::kThreads;
+  v.groups = specv::kGroups;
+  v.head_bytes_raw = static_cast<int>(sizeof(specv::SmemHead));
+  v.consumer_warps = specv::kConsumerWarps;
+  v.kernel[0] = reinterpret_cast<void*>(&specv::verify_accept_kernel<float, false>);
+  v.kernel[1] = reinterpret_cast<void*>(&specv::verify_accept_kernel<float, true>);
+  v.kernel[2] = reinterpret_cast<void*>(&specv::verify_accept_kernel<bf16_tag, false>);
+  v.kernel[3] = reinterpret_cast<void*>(&specv::verify_accept_kernel<bf16_tag, true>);
+  return v;
+}
+
+// Rounds with drafter logits may hold sampled lanes, whose sweep is bound by
+// instruction issue: 20 consumer warps hide more of its latency.  Greedy-only
+// rounds stream better with 16.  SPEC_VERIFY_WARPS=16|20 overrides.
+int pick_variant(bool with_draft) {
+  const int w = env_int("SPEC_VERIFY_WARPS", 0);
+  if (w == 16) return 0;
+  if (w == 20) return 1;
+  return with_draft ? 1 : 0;
+}
+
+const KernelVariant& variant(int which) {
+  static const KernelVariant kVariants[2] = {w16_variant(), w20_variant()};
+  return kVariants[which];
 }
 
 int kernel_index(int dtype, bool aligned) { return dtype * 2 + (aligned ? 1 : 0); }
-
-void* pick_verify_kernel(int dtype, bool aligned) {
-  if (dtype == SPEC_BF16) return aligned ? verify_kernel_ptr<bf16_tag, true>() : verify_kernel_ptr<bf16_tag, false>();
-  return aligned ? verify_kernel_ptr<float, true>() : verify_kernel_ptr<float, false>();
-}
 
 bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -143,7 +165,7 @@ constexpr int kFitCache = 128;
 ClusterFit g_fit[kFitCache];
 int g_fit_n = 0;
 
-int max_active_clusters(int dev, void* kernel, int cluster, int smem) {
+int max_active_clusters(int dev, void* kernel, int threads, int cluster, int smem) {
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     for (int i = 0; i < g_fit_n; ++i)
@@ -153,7 +175,7 @@ int max_active_clusters(int dev, void* kernel, int cluster, int smem) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
-  cfg.blockDim = dim3(specv::kThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -196,15 +218,16 @@ __global__ void round_uniforms_kernel(uint64_t seed, uint32_t lane_base, int32_t
 // must fit into one GPU processing cluster, smaller clusters until one fits.
 // When every lane could run at once (few lanes) the cluster also shrinks until
 // all of them fit together, so that no lane waits for a second wave.
-int resolve_shape(DeviceCache* dc, int dev, int lanes, int rows, int V, int dtype, bool aligned, VerifyShape* out,
-                  void** kernel_out) {
+int resolve_shape(DeviceCache* dc, int dev, int which, int lanes, int rows, int V, int dtype, bool aligned,
+                  VerifyShape* out, void** kernel_out) {
+  const KernelVariant& kv = variant(which);
   const int esize = (dtype == SPEC_BF16) ? 2 : 4;
-  VerifyShape s = choose_shape(lanes, rows, V, esize, aligned, dc->sms, dc->smem_optin, 0);
+  VerifyShape s = choose_shape(kv, lanes, rows, V, esize, aligned, dc->sms, dc->smem_optin, 0);
   if (s.smem > dc->smem_optin) return SPEC_ERR_UNSUPPORTED;
-  void* kernel = pick_verify_kernel(dtype, aligned);
+  void* kernel = kv.kernel[kernel_index(dtype, aligned)];
   {
     std::lock_guard<std::mutex> lock(g_mutex);
-    bool& done = dc->verify_attr[kernel_index(dtype, aligned)];
+    bool& done = dc->verify_attr[which * 4 + kernel_index(dtype, aligned)];
     if (!done) {
       if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dc->smem_optin) !=
               cudaSuccess ||
@@ -215,11 +238,11 @@ int resolve_shape(DeviceCache* dc, int dev, int lanes, int rows, int V, int dtyp
   }
   const bool forced = env_int("SPEC_VERIFY_CLUSTER", 0) > 0;
   for (;;) {
-    const int active = max_active_clusters(dev, kernel, s.cluster, s.smem);
+    const int active = max_active_clusters(dev, kernel, kv.threads, s.cluster, s.smem);
     s.active = active;
     const bool few = static_cast<int64_t>(lanes) * s.cluster <= 2LL * dc->sms;
     if (s.cluster == 1 || (active > 0 && (forced || !few || active >= lanes))) break;
-    s = choose_shape(lanes, rows, V, esize, aligned, dc->sms, dc->smem_optin, smaller_cluster(s.cluster));
+    s = choose_shape(kv, lanes, rows, V, esize, aligned, dc->sms, dc->smem_optin, smaller_cluster(s.cluster));
   }
   *out = s;
   if (kernel_out) *kernel_out = kernel;
@@ -267,18 +290,19 @@ const char* spec_status_string(int status) {
   }
 }
 
-int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype dtype, int32_t* cluster_ctas,
-                             int32_t* threads, int32_t* slice, int32_t* smem_bytes) {
+int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype dtype, int32_t with_draft,
+                             int32_t* cluster_ctas, int32_t* threads, int32_t* slice, int32_t* smem_bytes) {
   if (lanes <= 0 || rows < lanes || V <= 0 || (dtype != SPEC_F32 && dtype != SPEC_BF16))
     return SPEC_ERR_INVALID_ARG;
   DeviceCache* dc = nullptr;
   int dev = 0;
   if (device_cache(&dc, &dev) != SPEC_OK) return SPEC_ERR_CUDA;
   VerifyShape s{};
-  const int rc = resolve_shape(dc, dev, lanes, rows, V, dtype, true, &s, nullptr);
+  const int which = pick_variant(with_draft != 0);
+  const int rc = resolve_shape(dc, dev, which, lanes, rows, V, dtype, true, &s, nullptr);
   if (rc != SPEC_OK) return rc;
   if (cluster_ctas) *cluster_ctas = s.cluster;
-  if (threads) *threads = specv::kThreads;
+  if (threads) *threads = variant(which).threads;
   if (slice) *slice = s.slice;
   if (smem_bytes) *smem_bytes = s.smem;
   return SPEC_OK;
@@ -304,7 +328,8 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
                        ((a->ld * esize) % 16 == 0);
   VerifyShape s{};
   void* kernel = nullptr;
-  const int rc = resolve_shape(dc, dev, a->lanes, a->rows, a->V, a->dtype, aligned, &s, &kernel);
+  const int which = pick_variant(a->draft_logits != nullptr);
+  const int rc = resolve_shape(dc, dev, which, a->lanes, a->rows, a->V, a->dtype, aligned, &s, &kernel);
   if (rc != SPEC_OK) return rc;
 
   specv::VerifyParams p{};
@@ -324,6 +349,7 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
   p.lane_status = a->lane_status;
   p.row_stats = a->row_stats;
   p.lane_base = a->lane_base;
+  p.flags = a->flags;
   p.cluster = s.cluster;
   p.slice = s.slice;
   p.slot_bytes = s.slot_bytes;
@@ -335,7 +361,7 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(s.cluster * a->lanes), 1, 1);
-  cfg.blockDim = dim3(specv::kThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(variant(which).threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(s.smem);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attrs[2];

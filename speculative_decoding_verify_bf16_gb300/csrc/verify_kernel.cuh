@@ -138,6 +138,7 @@ struct VerifyParams {
   int32_t nslots;
   int32_t head_bytes;  // offset of the ring in dynamic shared memory
   int32_t order_by_cost;  // clusters take lanes in order of decreasing cost (more lanes than fit at once)
+  uint32_t flags;         // SPEC_VERIFY_* flags of spec_verify_args
 };
 
 // ---------------------------------------------------------------------------
@@ -807,7 +808,10 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     fence_mbar_init();
   }
   if (tid <= kMaxDrafts) sh.gkey[tid] = 0ull;
-  griddep_wait();
+  // The lane metadata may be read before the wait for the previous kernel on
+  // the stream only when the caller says that kernel did not write it.
+  const bool meta_early = (p.flags & SPEC_VERIFY_META_BEFORE_WAIT) != 0u;
+  if (!meta_early) griddep_wait();
   if (p.order_by_cost) b = lane_of_rank(p, sh, b);
 
   // ---- lane metadata (read by every thread; one transaction per warp) ----
@@ -826,6 +830,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   }
   const int nstreams = (status != SPEC_OK) ? 0 : (sampled ? 2 * k + 1 : k + 1);
   const float c = sampled ? __fdiv_rn(kLog2e, temp) : 0.f;
+  if (meta_early) griddep_wait();  // logits and outputs only after the previous kernel
   // Let the next kernel on the stream start its set-up now.  It cannot begin
   // before every CTA of this grid has started and issued this, and it reads
   // nothing of ours before its own griddepcontrol.wait, which waits for this

@@ -36,7 +36,7 @@ def logits_to_numpy(t, vocab):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(r, stats=True, stream=None):
+def run_gpu(r, stats=True, stream=None, meta_before_wait=False):
     """Verify round r (device tensors) through the binding; numpy results."""
     dev = r.target.device
     lanes, rows = r.lanes, r.rows
@@ -48,7 +48,7 @@ def run_gpu(r, stats=True, stream=None):
     draft = r.draft[:, :r.vocab] if r.draft is not None else None
     sv.spec_verify_accept(target, draft, r.draft_tokens, r.draft_lens, r.row_offsets,
                           r.temperatures, r.seed, committed, out_tokens, status, row_stats,
-                          stream=stream, rows=rows)
+                          stream=stream, rows=rows, meta_before_wait=meta_before_wait)
     torch.cuda.synchronize()
     res = {"committed": committed.cpu().numpy(), "out_tokens": out_tokens.cpu().numpy(),
            "lane_status": status.cpu().numpy()}

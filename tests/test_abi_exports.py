@@ -1,5 +1,6 @@
 """The C-ABI library loads and exports what include/*.h declares (no GPU needed)."""
 
+import ctypes
 import glob
 import os
 import re
@@ -72,3 +73,34 @@ def test_calls_with_bad_arguments_fail_on_the_host(lib):
     assert lib.spec_commit_state(None, None, None, -1, 1, 16, 16, 16, 16, None, None) == \
         sv.SPEC_ERR_INVALID_ARG
     assert lib.spec_commit_state(None, None, None, 0, 1, 16, 16, 16, 16, None, None) == sv.SPEC_OK
+
+
+def _c_layout(struct, fields, tmp_path):
+    """sizeof and offsetof of `struct`'s `fields` from a C program built against the headers."""
+    src = tmp_path / "layout.c"
+    body = "".join(f'  printf("%zu\\n", offsetof({struct}, {f}));\n' for f in fields)
+    src.write_text(f'#include <stddef.h>\n#include <stdio.h>\n#include "spec_round_control.h"\n'
+                   f'int main(void) {{\n  printf("%zu\\n", sizeof({struct}));\n{body}  return 0;\n}}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    return vals[0], vals[1:]
+
+
+@pytest.mark.parametrize("struct,cls", [("spec_verify_args", sv._Args),
+                                        ("spec_accept_counts", sv._AcceptCounts),
+                                        ("spec_accept_rates", sv._AcceptRates)])
+def test_binding_structs_match_the_c_layout(struct, cls, tmp_path):
+    """The ctypes structures the binding passes have the C structs' size and field offsets."""
+    fields = [name for name, _ in cls._fields_]
+    size, offsets = _c_layout(struct, fields, tmp_path)
+    assert ctypes.sizeof(cls) == size
+    assert [getattr(cls, f).offset for f in fields] == offsets
+
+
+def test_binding_constants_match_the_header_defines():
+    text = "".join(open(p).read() for p in glob.glob(os.path.join(ROOT, "include", "*.h")))
+    defines = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(SPEC_\w+)\s+(\d+)u?\b", text)}
+    for name in ("SPEC_MAX_DRAFTS", "SPEC_VERIFY_META_BEFORE_WAIT", "SPEC_NGRAM_MAX_MATCH"):
+        assert getattr(sv, name) == defines[name], name

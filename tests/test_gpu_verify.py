@@ -287,17 +287,41 @@ def test_longest_first_lane_order_changes_nothing(monkeypatch, lanes, vocab, kma
         monkeypatch.setenv("SPEC_VERIFY_ORDER", order)
         runs[order] = run_gpu(r)
         compare(r, runs[order], orc)
+    # the order is also computed before the wait for the previous kernel
+    runs["early"] = run_gpu(r, meta_before_wait=True)
     for key in ("committed", "out_tokens", "lane_status"):
         np.testing.assert_array_equal(runs["0"][key], runs["1"][key], err_msg=key)
+        np.testing.assert_array_equal(runs["1"][key], runs["early"][key], err_msg=key)
+
+
+@pytest.mark.parametrize("sampled,dtype", [("mixed", "bf16"), ("none", "bf16"), ("all", "f32")])
+def test_both_kernel_builds_match_the_oracle(monkeypatch, sampled, dtype):
+    """Rounds with drafter logits run the 20-consumer-warp build of the kernel,
+    rounds without them the 16-warp build.  Forcing either build on either kind
+    of round must match the oracle; greedy lanes are bit-identical between the
+    two (the argmax does not depend on how the warps split the slice)."""
+    r = workloads.make_custom_round(58, DEV, lanes=11, vocab=50021, kmax=7, dtype=dtype, sampled=sampled)
+    orc = run_oracle(r)
+    runs = {}
+    for warps in ("16", "20"):
+        monkeypatch.setenv("SPEC_VERIFY_WARPS", warps)
+        shape = sv.spec_verify_launch_shape(r.lanes, r.rows, r.vocab, r.target.dtype)
+        assert shape["threads"] == (int(warps) + 2) * 32
+        runs[warps] = run_gpu(r)
+        compare(r, runs[warps], orc)
+    greedy = r.temperatures.cpu().numpy() <= 0
+    np.testing.assert_array_equal(runs["16"]["committed"][greedy], runs["20"]["committed"][greedy])
 
 
 @pytest.mark.parametrize("cluster,ring_kb,slot_kb", [("4", "75", "32"), ("12", "75", "32"), ("16", "88", "32"),
                                                       ("8", "40", "8"), ("2", "100", "32")])
-def test_back_to_back_graph_launches_are_identical(monkeypatch, cluster, ring_kb, slot_kb):
+@pytest.mark.parametrize("meta_early", [False, True], ids=["meta-after-wait", "meta-before-wait"])
+def test_back_to_back_graph_launches_are_identical(monkeypatch, cluster, ring_kb, slot_kb, meta_early):
     """50 launches captured in one CUDA graph (the kernels overlap through
     programmatic dependent launch), each into its own outputs: every launch
     must give the same results, equal to the oracle's.  Ring shapes that would
-    leave an odd number of slots are included on purpose."""
+    leave an odd number of slots are included on purpose; so is the launch
+    that reads the lane metadata before waiting for the previous kernel."""
     monkeypatch.setenv("SPEC_VERIFY_CLUSTER", cluster)
     monkeypatch.setenv("SPEC_VERIFY_RING_KB", ring_kb)
     monkeypatch.setenv("SPEC_VERIFY_SLOT_KB", slot_kb)
@@ -311,7 +335,8 @@ def test_back_to_back_graph_launches_are_identical(monkeypatch, cluster, ring_kb
 
     def launch(o):
         sv.spec_verify_accept(r.target, r.draft, r.draft_tokens, r.draft_lens, r.row_offsets,
-                              r.temperatures, r.seed, o[0], o[1], o[2], stream=torch.cuda.current_stream())
+                              r.temperatures, r.seed, o[0], o[1], o[2], stream=torch.cuda.current_stream(),
+                              meta_before_wait=meta_early)
 
     with torch.cuda.stream(stream):
         launch(outs[0])  # sets kernel attributes before capture
