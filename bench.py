@@ -689,6 +689,8 @@ def run_launch_only(args):
     out = torch.zeros(r.rows, dtype=torch.int32, device=device)
     status = torch.zeros(r.lanes, dtype=torch.int32, device=device)
     for i in range(args.launch_only):
+        # Profilers replay a launch after restoring memory with work of their
+        # own, so the metadata is read only after the wait here.
         sv.spec_verify_accept(r.target, r.draft, r.draft_tokens, r.draft_lens, r.row_offsets,
                               r.temperatures, r.seed, committed, out, status)
         if r.staged is not None:

@@ -367,14 +367,40 @@ __device__ __forceinline__ int vec_find(const uint4* sv, int vv, float m) {
 // also sum each group's exponentials relative to the group's own max
 // (fl(max * c) as reference, packed fp32 pairs), and fold the group sum into
 // the lane's running sum with one rescaling exp2.
-template <typename T, bool SAMPLED>
+//
+// LAZY (sampled rows whose max and argmax are not reported): once the lane
+// has a finite reference M (the max of the groups taken so far), a group's
+// exponentials are summed against M directly, with no group max.  The sum of
+// 32 terms is at most 32 while no element exceeds M; a sum above 2^64, +inf
+// or NaN sends the group through the exact path above instead, which raises
+// M, rescales, and flags NaN and +inf.  M then stays an element value at or
+// below the row max, and every later use of the partial (merges, the
+// acceptance test, the draw) needs only that the sum is relative to
+// fl(M * c).
+constexpr float kLazySumLimit = 18446744073709551616.f;  // 2^64
+
+template <typename T, bool SAMPLED, bool LAZY = false>
 __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int ve, int ebase, float c,
                                           int lane) {
   float M = -INFINITY, nanacc = -INFINITY;
   float S = 0.f;  // sampled: sum relative to scaled_ref(M)
+  float rM = 0.f; // LAZY: scaled_ref(M) while M is finite
   int gv = -1;    // first vector holding M
   const unsigned long long c2 = f2_pack(c, c);
   auto group = [&](const uint4 (&x)[4], int v) {
+    if (LAZY && M != -INFINITY) {
+      const unsigned long long nmr2 = f2_pack(-rM, -rM);
+      unsigned long long acc = 0ull;  // (+0, +0)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc = vec_exp_acc<T>(x[u], c2, nmr2, acc);
+      float lo, hi;
+      f2_unpack(acc, lo, hi);
+      const float sg = lo + hi;
+      if (sg <= kLazySumLimit) {
+        S += sg;
+        return;
+      }
+    }
     uint32_t h[4];
     group_vec_max<T>(x, h);
     const float gm = group_max_nan<T>(h);
@@ -395,6 +421,7 @@ __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int v
       // A new running max (rare after the first groups): the first vector of
       // the group that holds it.
       M = gm;
+      if (LAZY) rM = scaled_ref(M, c);
       gv = v + 96;
 #pragma unroll
       for (int u = 2; u >= 0; --u)
@@ -416,7 +443,8 @@ __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int v
   if (nanacc != nanacc || nanacc == INFINITY) a.bad = 1;
   if (M == -INFINITY) return;
   if (SAMPLED) {
-    const int e = (M >= a.m) ? ebase + vec_find<T>(sv, gv, M) : INT_MAX;  // index only matters then
+    // LAZY: any element index marks the partial as holding elements
+    const int e = LAZY ? ebase : (M >= a.m) ? ebase + vec_find<T>(sv, gv, M) : INT_MAX;
     merge_part<true>(a.m, a.s, a.idx, M, S, e, c);
   } else if (M > a.m) {
     acc_raise<false>(a, M, ebase + vec_find<T>(sv, gv, M), c);
@@ -849,7 +877,9 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   // sampled lanes their pass-2 slice sums.  Announced before this CTA arrives
   // on the cluster barrier, so before any peer can push.
   // (A greedy lane's peers send 16 bytes per row to the leader only.)
-  if (tid == 0) {
+  // The thread that initialised these barriers arms them: no other thread is
+  // ordered after their initialisation before the barrier below.
+  if (tid == 32 + kMaxSlots) {
     const bool receives = sampled || leader;
     mbar_arrive_expect_tx(&sh.xbar, receives ? static_cast<uint32_t>((C - 1) * nstreams * 16) : 0u);
     if (sampled) {
@@ -926,6 +956,8 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       for (int s = 0; s < nstreams; ++s)
         if (lane == 0) sh.wpart[s][warp] = identity_partial();
     bool ok = true;
+    // Sampled rows report their exact max and argmax only into row_stats.
+    const bool exact_stats = p.row_stats != nullptr;
     if (ALIGNED && body > 0) {
       const int nch = (body + slot_elems - 1) / slot_elems;  // chunks per row
       int cur = -1;
@@ -959,7 +991,8 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
         const int nvec = min(slot_elems, body - c0) / kVec;
         const int per = (nvec + kPieces - 1) / kPieces;
         const int vb = min(nvec, q * per), ve = min(nvec, vb + per);
-        if (sampled) acc_range<T, true>(a, sv, vb, ve, v0 + c0, c, lane);
+        if (sampled && exact_stats) acc_range<T, true, false>(a, sv, vb, ve, v0 + c0, c, lane);
+        else if (sampled) acc_range<T, true, true>(a, sv, vb, ve, v0 + c0, c, lane);
         else acc_range<T, false>(a, sv, vb, ve, v0 + c0, c, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.empty[slot]);

@@ -40,14 +40,16 @@ SMALL_CASES = [
 ]
 
 
+@pytest.mark.parametrize("stats", [True, False], ids=["stats", "nostats"])
 @pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: f"V{c[0]}-k{c[1]}-B{c[2]}-{c[3]}-{c[4]}")
-def test_small_shapes_match_oracle(case):
+def test_small_shapes_match_oracle(case, stats):
+    """Without row_stats, sampled rows take the sweep that needs no exact max."""
     vocab, kmax, lanes, dtype, sampled, fixed_k, seed = case
     r = workloads.make_custom_round(seed, DEV, lanes=lanes, vocab=vocab, kmax=kmax, dtype=dtype,
                                     sampled=sampled, fixed_k=fixed_k)
-    gpu = run_gpu(r)
+    gpu = run_gpu(r, stats=stats)
     orc = run_oracle(r)
-    compare(r, gpu, orc)
+    compare(r, gpu, orc, check_stats=stats)
 
 
 @pytest.mark.parametrize("ld_extra", [8, 5, 64])
@@ -187,27 +189,62 @@ def _tiny_round(vocab=64, k=3, lanes=4, temp=0.0, seed=3):
                                        sampled="none" if temp <= 0 else "all", fixed_k=True)
 
 
-def test_nonfinite_rows_fail_only_their_lane():
-    r = _tiny_round(lanes=5, temp=1.0)
+@pytest.mark.parametrize("stats", [True, False], ids=["stats", "nostats"])
+@pytest.mark.parametrize("vocab", [64, 20000])
+def test_nonfinite_rows_fail_only_their_lane(stats, vocab):
+    r = _tiny_round(vocab=vocab, lanes=5, temp=1.0)
     off = r.row_offsets.cpu().numpy()
     r.target[off[1] + 2, 7] = float("nan")
-    r.target[off[2] + 0, 3] = float("inf")
+    r.target[off[2] + 0, vocab - 3] = float("inf")
     r.target[off[3] + 1, :] = float("-inf")
-    r.draft[off[4] + 0, 5] = float("nan")          # a drafter row that is read
+    r.draft[off[4] + 0, vocab // 2] = float("nan")  # a drafter row that is read
     r.draft[off[0] + 3, 5] = float("nan")          # the lane's last drafter row: never read
-    gpu, orc = run_gpu(r), run_oracle(r)
+    gpu, orc = run_gpu(r, stats=stats), run_oracle(r)
     assert gpu["lane_status"].tolist() == [0, 4, 4, 4, 4]
-    compare(r, gpu, orc)
+    compare(r, gpu, orc, check_stats=stats)
 
 
-def test_negative_infinity_logits_are_allowed():
+@pytest.mark.parametrize("stats", [True, False], ids=["stats", "nostats"])
+def test_negative_infinity_logits_are_allowed(stats):
     r = _tiny_round(lanes=4, temp=0.0)
     r.target[:, ::3] = float("-inf")
-    compare(r, run_gpu(r), run_oracle(r))
+    compare(r, run_gpu(r, stats=stats), run_oracle(r), check_stats=stats)
     r = _tiny_round(lanes=4, temp=1.0)
     r.target[:, ::3] = float("-inf")
     r.draft[:, 1::4] = float("-inf")
-    compare(r, run_gpu(r), run_oracle(r))
+    compare(r, run_gpu(r, stats=stats), run_oracle(r), check_stats=stats)
+    # a sampled lane whose rows start with a long run of -inf (no reference for a while)
+    r = _tiny_round(vocab=30000, lanes=3, temp=0.8)
+    r.target[:, :17000] = float("-inf")
+    r.draft[:, :9000] = float("-inf")
+    compare(r, run_gpu(r, stats=stats), run_oracle(r), check_stats=stats)
+
+
+@pytest.mark.parametrize("temp", [0.02, 0.3, 5.0])
+def test_rising_and_widely_spread_rows_without_row_stats(temp):
+    """Rows whose logits rise along the vocabulary (every group exceeds the
+    reference the sum was taken against) or spread over thousands of log2
+    units at low temperature: the sampled sweep that skips the exact max must
+    still match the oracle."""
+    lanes, k, vocab = 6, 4, 40000
+    r = workloads.make_custom_round(91, DEV, lanes=lanes, vocab=vocab, kmax=k, dtype="bf16", sampled="all",
+                                    fixed_k=True)
+    rise = torch.linspace(-30.0, 30.0, vocab, device=DEV)
+    for b in range(0, lanes, 2):   # even lanes: rising rows, odd lanes: very wide noise
+        rows = slice(b * (k + 1), (b + 1) * (k + 1))
+        r.target[rows] = (rise + r.target[rows].float() * 0.1).to(r.target.dtype)
+        r.draft[rows] = (rise + r.draft[rows].float() * 0.1).to(r.draft.dtype)
+    for b in range(1, lanes, 2):
+        rows = slice(b * (k + 1), (b + 1) * (k + 1))
+        r.target[rows] = (r.target[rows].float() * 40.0).to(r.target.dtype)
+        r.draft[rows] = (r.target[rows].float() + 0.1 * torch.randn_like(r.draft[rows].float())).to(r.draft.dtype)
+    # drafts at the drafter's mode, so that p(d) and q(d) stay far from fp64 underflow
+    pos = torch.arange(r.rows, device=DEV) % (k + 1) < k
+    r.draft_tokens[pos] = r.draft.float().argmax(dim=1).to(torch.int32)[pos]
+    r.temperatures.fill_(temp)
+    orc = run_oracle(r)
+    compare(r, run_gpu(r, stats=False), orc, check_stats=False)
+    compare(r, run_gpu(r, stats=True), orc, check_stats=True)
 
 
 def test_token_range_layout_and_unsupported_statuses():
