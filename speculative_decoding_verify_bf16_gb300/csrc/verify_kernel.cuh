@@ -57,7 +57,7 @@ constexpr int kDrawRound = 256;  // elements per warp per pass-2 round (32 lanes
 #endif
 constexpr int kPieces = SPEC_VERIFY_PIECES;  // warps sharing one chunk of the ring
 #ifndef SPEC_VERIFY_UNROLL
-#define SPEC_VERIFY_UNROLL 2
+#define SPEC_VERIFY_UNROLL 1
 #endif
 constexpr int kGroupUnroll = SPEC_VERIFY_UNROLL;  // groups per iteration of the sweep loop
 // Consumer warps form kGroups groups of kPieces; group g takes the chunks
@@ -387,20 +387,17 @@ __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int v
   float rM = 0.f; // LAZY: scaled_ref(M) while M is finite
   int gv = -1;    // first vector holding M
   const unsigned long long c2 = f2_pack(c, c);
-  auto group = [&](const uint4 (&x)[4], int v) {
-    if (LAZY && M != -INFINITY) {
-      const unsigned long long nmr2 = f2_pack(-rM, -rM);
-      unsigned long long acc = 0ull;  // (+0, +0)
+  // LAZY: the group's exponentials against the lane's reference.
+  auto lazy_sum = [&](const uint4 (&x)[4]) -> float {
+    const unsigned long long nmr2 = f2_pack(-rM, -rM);
+    unsigned long long acc = 0ull;  // (+0, +0)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) acc = vec_exp_acc<T>(x[u], c2, nmr2, acc);
-      float lo, hi;
-      f2_unpack(acc, lo, hi);
-      const float sg = lo + hi;
-      if (sg <= kLazySumLimit) {
-        S += sg;
-        return;
-      }
-    }
+    for (int u = 0; u < 4; ++u) acc = vec_exp_acc<T>(x[u], c2, nmr2, acc);
+    float lo, hi;
+    f2_unpack(acc, lo, hi);
+    return lo + hi;
+  };
+  auto exact = [&](const uint4 (&x)[4], int v) {
     uint32_t h[4];
     group_vec_max<T>(x, h);
     const float gm = group_max_nan<T>(h);
@@ -428,12 +425,45 @@ __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int v
         if (unpack_max<T>(h[u]) == gm) gv = v + 32 * u;
     }
   };
+  auto group = [&](const uint4 (&x)[4], int v) {
+    if (LAZY && M != -INFINITY) {
+      const float sg = lazy_sum(x);
+      if (sg <= kLazySumLimit) {
+        S += sg;
+        return;
+      }
+    }
+    exact(x, v);
+  };
   int v = vb + lane;
+  if constexpr (LAZY) {
+    // A tight loop of lazily summed groups; a group it cannot take (no
+    // reference yet, or a sum out of range) leaves it for the exact path,
+    // which is kept out of the loop body.
+    for (;;) {
+      if (M != -INFINITY) {
 #pragma unroll kGroupUnroll
-  for (; v + 96 < ve; v += 128) {
-    uint4 x[4];
-    load_group<T, false>(sv, v, ve, x);
-    group(x, v);
+        for (; v + 96 < ve; v += 128) {
+          uint4 x[4];
+          load_group<T, false>(sv, v, ve, x);
+          const float sg = lazy_sum(x);
+          if (!(sg <= kLazySumLimit)) break;
+          S += sg;
+        }
+      }
+      if (v + 96 >= ve) break;
+      uint4 x[4];
+      load_group<T, false>(sv, v, ve, x);
+      exact(x, v);
+      v += 128;
+    }
+  } else {
+#pragma unroll kGroupUnroll
+    for (; v + 96 < ve; v += 128) {
+      uint4 x[4];
+      load_group<T, false>(sv, v, ve, x);
+      group(x, v);
+    }
   }
   if (v < ve) {
     uint4 x[4];
