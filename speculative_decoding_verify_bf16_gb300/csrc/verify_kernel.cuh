@@ -1245,6 +1245,14 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
 #endif
   const int seg = ((span + kConsumerWarps - 1) / kConsumerWarps + SPEC_VERIFY_SEG_ROUND - 1) /
                   SPEC_VERIFY_SEG_ROUND * SPEC_VERIFY_SEG_ROUND;
+  // Each warp keeps the weight sum of every round of its segment in the ring
+  // (free after pass 1), so that the warp holding the crossing later re-reads
+  // one round instead of walking its segment.  Unaligned launches have no
+  // ring; they, and segments with more rounds than fit, walk the segment.
+  const int seg_rounds = (seg + kDrawRound - 1) / kDrawRound;
+  float* round_sums = reinterpret_cast<float*>(ring);
+  const bool keep_rounds = ALIGNED && static_cast<int64_t>(seg_rounds) * kConsumerWarps * 4 <=
+                                          static_cast<int64_t>(nslots) * p.slot_bytes;
   auto make_coef = [&]() {
     DrawCoef kc;
     const Partial pt = sh.fin[2 * draw_row];
@@ -1293,7 +1301,9 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             if (w[i] > 0.f) last = e + i;
-          segw = __fadd_rn(segw, warp_sum_xor(cum[7]));
+          const float R = warp_sum_xor(cum[7]);
+          if (keep_rounds && lane == 0) round_sums[warp * seg_rounds + (base - s0) / kDrawRound + u] = R;
+          segw = __fadd_rn(segw, R);
         }
       }
       last = warp_max_int(last);
@@ -1376,10 +1386,28 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       const DrawCoef kc = make_coef();
       const uint8_t* trow = p.target + static_cast<int64_t>(off + draw_row) * p.ld_bytes;
       const float tau1 = __fsub_rn(tau, q);
-      const int s0 = v0 + warp * seg;
-      const int s1 = min(v1, s0 + seg);
+      int s0 = v0 + warp * seg;
+      int s1 = min(v1, s0 + seg);
       float run = 0.f;
       int found = -1;
+      if (keep_rounds) {
+        // The round whose sum takes the running total past tau1, from the
+        // sums the same warp took in the same order; only it is re-read.
+        const int nr = (s1 - s0 + kDrawRound - 1) / kDrawRound;
+        int r = 0;
+        for (; r < nr; ++r) {
+          const float R = round_sums[warp * seg_rounds + r];
+          const float next = __fadd_rn(run, R);
+          if (next > tau1) break;
+          run = next;
+        }
+        if (r == nr) {
+          s0 = s1;  // no crossing: the segment's last positive weight below
+        } else {
+          s0 += r * kDrawRound;
+          s1 = min(s1, s0 + kDrawRound);
+        }
+      }
       for (int bbase = s0; bbase < s1 && found < 0; bbase += kDrawBatch * kDrawRound) {
         Raw8<T> rt[kDrawBatch], rq[kDrawBatch];
 #pragma unroll

@@ -295,6 +295,22 @@ def test_identical_draft_and_target_accepts_everything():
     compare(r, gpu, orc)
 
 
+@pytest.mark.parametrize("cluster,vocab", [("1", 262144), ("2", 151936), ("4", 262144), ("3", 99991)])
+def test_draws_deep_in_long_segments(monkeypatch, cluster, vocab):
+    """Small clusters on large vocabularies give every warp a pass-2 segment of
+    many 256-element rounds (up to 52).  The warp that holds the crossing finds
+    its round from the round sums kept in the sum phase and re-reads only that
+    round; over many seeds the crossings fall in every part of the segments.
+    Drawn tokens must match the oracle's inverse-CDF draws."""
+    monkeypatch.setenv("SPEC_VERIFY_CLUSTER", cluster)
+    for seed in range(3):
+        r = workloads.make_custom_round(700 + seed, DEV, lanes=6, vocab=vocab, kmax=3, dtype="bf16", sampled="all",
+                                        fixed_k=True, sigma=0.5, spike=0.0, alpha=0.3)
+        orc = run_oracle(r)
+        compare(r, run_gpu(r, stats=False), orc, check_stats=False)
+        compare(r, run_gpu(r, stats=True), orc, check_stats=True)
+
+
 def test_results_do_not_depend_on_the_cluster_shape(monkeypatch):
     r = workloads.make_custom_round(31, DEV, lanes=6, vocab=70000, kmax=7, dtype="bf16", sampled="mixed")
     ref = run_gpu(r)
