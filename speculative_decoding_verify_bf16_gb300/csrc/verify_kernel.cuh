@@ -1193,6 +1193,17 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     if (lane == 0) {
       sh.scan_n = n;
       sh.scan_mode = (st == SPEC_OK) ? mode : kNoDraw;
+      // The draw re-reads this CTA's slice of one row pair; on rounds larger
+      // than L2 part of it may have left L2 since pass 1: fetch it back now.
+      if (ALIGNED && st == SPEC_OK && body > 0) {
+        const int drow = (mode == kResidual) ? n : k;
+        const int64_t col = static_cast<int64_t>(v0) * kEsize;
+        bulk_prefetch_l2(p.target + static_cast<int64_t>(off + drow) * p.ld_bytes + col,
+                         static_cast<uint32_t>(body * kEsize));
+        if (mode == kResidual)
+          bulk_prefetch_l2(p.draft + static_cast<int64_t>(off + n) * p.ld_bytes + col,
+                           static_cast<uint32_t>(body * kEsize));
+      }
     }
 
     // ---- outputs (leader) ----
@@ -1282,18 +1293,23 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       const int s1 = min(v1, s0 + seg);
       float segw = 0.f;
       int last = -1;
-      for (int base = s0; base < s1; base += kDrawBatch * kDrawRound) {
-        Raw8<T> rt[kDrawBatch], rq[kDrawBatch];
+      // Software-pipelined in two halves of kDrawBatch rounds: the loads of
+      // the next half are in flight while this half is computed.
+      constexpr int kHalf = kDrawBatch / 2;
+      Raw8<T> rtA[kHalf], rqA[kHalf], rtB[kHalf], rqB[kHalf];
+      auto load_half = [&](Raw8<T> (&rt)[kHalf], Raw8<T> (&rq)[kHalf], int base) {
 #pragma unroll
-        for (int u = 0; u < kDrawBatch; ++u) {
+        for (int u = 0; u < kHalf; ++u) {
           const int e = base + u * kDrawRound + lane * 8;
           if (base + u * kDrawRound < s1) {
             load_raw8<T, ALIGNED>(trow, e, s1, rt[u]);
             if (kc.residual) load_raw8<T, ALIGNED>(qrow, e, s1, rq[u]);
           }
         }
+      };
+      auto sum_half = [&](const Raw8<T> (&rt)[kHalf], const Raw8<T> (&rq)[kHalf], int base) {
 #pragma unroll
-        for (int u = 0; u < kDrawBatch; ++u) {
+        for (int u = 0; u < kHalf; ++u) {
           if (base + u * kDrawRound >= s1) break;
           float w[8], cum[8];
           const int e = base + u * kDrawRound + lane * 8;
@@ -1304,6 +1320,23 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
           const float R = warp_sum_xor(cum[7]);
           if (keep_rounds && lane == 0) round_sums[warp * seg_rounds + (base - s0) / kDrawRound + u] = R;
           segw = __fadd_rn(segw, R);
+        }
+      };
+      constexpr int kStep = kHalf * kDrawRound;
+      if (seg_rounds <= kDrawBatch) {
+        // A segment of one batch: every load first, then the sums.
+        if (s0 < s1) load_half(rtA, rqA, s0);
+        if (s0 + kStep < s1) load_half(rtB, rqB, s0 + kStep);
+        if (s0 < s1) sum_half(rtA, rqA, s0);
+        if (s0 + kStep < s1) sum_half(rtB, rqB, s0 + kStep);
+      } else {
+        if (s0 < s1) load_half(rtA, rqA, s0);
+        for (int base = s0; base < s1; base += 2 * kStep) {
+          if (base + kStep < s1) load_half(rtB, rqB, base + kStep);
+          sum_half(rtA, rqA, base);
+          if (base + kStep >= s1) break;
+          if (base + 2 * kStep < s1) load_half(rtA, rqA, base + 2 * kStep);
+          sum_half(rtB, rqB, base + kStep);
         }
       }
       last = warp_max_int(last);
