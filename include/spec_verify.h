@@ -213,6 +213,22 @@ int spec_round_uniforms(uint64_t seed, uint32_t lane_base, int32_t lanes, int32_
 const char* spec_status_string(int status);
 
 /*
+ * Launch-shape overrides.  Environment variables read on every call, for
+ * experiments and tests; normal use needs none of them:
+ *   SPEC_VERIFY_CLUSTER=C    CTAs per lane (1..16); shrunk only if it cannot be scheduled
+ *   SPEC_VERIFY_SLOT_KB=K    largest ring slot in KB (default 40)
+ *   SPEC_VERIFY_RING_KB=K    ring size in KB (default: all shared memory left)
+ *   SPEC_VERIFY_ORDER=0|1    clusters take lanes longest first (default: only when
+ *                            the launch has more lanes than resident clusters)
+ *   SPEC_VERIFY_WARPS=16|20  which build of the verify kernel runs (see spec_verify_accept)
+ *   SPEC_COMMIT_CHUNK_KB, SPEC_COMMIT_NBUF, SPEC_COMMIT_CTAS_PER_SM
+ *                            copy shape of spec_commit_state (defaults 32, 6, 1)
+ * Greedy lanes and the commit give the same results under every override;
+ * sampled lanes stay within the stated tolerance of the definition (their
+ * fp32 sums are added in an order that follows the shape).
+ */
+
+/*
  * spec_verify_launch_shape -- the launch spec_verify_accept would use.
  *
  * Host-only.  Reports the CTAs per lane (one thread-block cluster per lane),

@@ -248,3 +248,34 @@ def test_penalties_argument_errors():
     assert lib.spec_apply_penalties(None, 1, 9, 10, 0, *([None] * 9)) == sv.SPEC_ERR_INVALID_ARG
     assert lib.spec_apply_penalties(None, 7, 10, 10, 0, *([None] * 9)) == sv.SPEC_ERR_INVALID_ARG
     assert lib.spec_apply_penalties(None, 1, 10, 10, 0, *([None] * 9)) == sv.SPEC_OK
+
+
+def test_mean_committed_count_follows_the_closed_form():
+    """Greedy rounds whose drafts equal the row argmax independently with
+    probability alpha (a uniform token otherwise, which matches with
+    probability 1/V): the committed count is a truncated geometric variable,
+    E[c] = (1 - a^(k+1)) / (1 - a) with a = alpha + (1 - alpha) / V
+    (strata2signal "Tokens a round" gives the closed form for independent
+    guesses).  The device's mean over 2048 lanes must lie within four
+    standard errors of it, and the alpha implied by the device counts within
+    four standard errors of a."""
+    lanes, k, vocab, alpha = 2048, 7, 1000, 0.8
+    r = workloads.make_custom_round(555, DEV, lanes=lanes, vocab=vocab, kmax=k, dtype="bf16", sampled="none",
+                                    fixed_k=True, alpha=alpha)
+    g = run_gpu(r, stats=False)
+    assert (g["lane_status"] == 0).all()
+    a = alpha + (1 - alpha) / vocab
+    n = np.arange(k + 1)
+    pmf = np.append(a ** n[:-1] * (1 - a), a ** k)          # P(n accepted), n = 0..k
+    mean = float((pmf * (n + 1)).sum())
+    assert abs(mean - (1 - a ** (k + 1)) / (1 - a)) < 1e-12
+    sd = float(np.sqrt((pmf * (n + 1 - mean) ** 2).sum()))
+    got = float(g["committed"].mean())
+    assert abs(got - mean) < 4 * sd / np.sqrt(lanes), (got, mean, sd)
+    counts = sv.new_accept_counts(1, DEV)
+    sv.spec_accept_counts_update(torch.tensor(g["committed"], device=DEV), r.draft_lens,
+                                 torch.tensor(g["lane_status"], device=DEV), counts)
+    rates = sv.spec_accept_rates_from_counts(counts[0])
+    # each guess j > 0 is reached by ~lanes * a^j rounds; the pooled estimate of a
+    # from slot survival has a standard error below sqrt(a (1 - a) / lanes)
+    assert abs(rates["given_previous"][0] - a) < 4 * np.sqrt(a * (1 - a) / lanes), rates
