@@ -222,7 +222,7 @@ const char* spec_status_string(int status);
  *                            the launch has more lanes than resident clusters)
  *   SPEC_VERIFY_WARPS=16|20  which build of the verify kernel runs (see spec_verify_accept)
  *   SPEC_COMMIT_CHUNK_KB, SPEC_COMMIT_NBUF, SPEC_COMMIT_CTAS_PER_SM
- *                            copy shape of spec_commit_state (defaults 32, 6, 1)
+ *                            copy shape of spec_commit_state (defaults 32, 2, 3)
  * Greedy lanes and the commit give the same results under every override;
  * sampled lanes stay within the stated tolerance of the definition (their
  * fp32 sums are added in an order that follows the shape).

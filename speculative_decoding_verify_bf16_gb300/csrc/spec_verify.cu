@@ -423,9 +423,12 @@ int spec_commit_state(const void* staged, void* live, const int32_t* committed, 
   void* kernel = nullptr;
 
   if (aligned) {
+    // Three CTAs per SM, each one thread driving two 32 KB buffers: more
+    // independent issuers beat deeper queues (one CTA with six buffers ran
+    // at 93 % of the measured copy bandwidth, this shape at 98 %).
     int chunk = env_int("SPEC_COMMIT_CHUNK_KB", 32) * 1024;
-    int nbuf = env_int("SPEC_COMMIT_NBUF", 6);
-    int per_sm = env_int("SPEC_COMMIT_CTAS_PER_SM", 1);
+    int nbuf = env_int("SPEC_COMMIT_NBUF", 2);
+    int per_sm = env_int("SPEC_COMMIT_CTAS_PER_SM", 3);
     if (nbuf < 2) nbuf = 2;
     if (nbuf > specv::kCommitMaxBufs) nbuf = specv::kCommitMaxBufs;
     if (per_sm < 1) per_sm = 1;
