@@ -379,6 +379,9 @@ __device__ __forceinline__ int vec_find(const uint4* sv, int vv, float m) {
 // fl(M * c).
 constexpr float kLazySumLimit = 18446744073709551616.f;  // 2^64
 
+// Ring slots up to this size are filled by one issuing lane per consumer group.
+constexpr int kParallelIssueSlotBytes = 8192;
+
 template <typename T, bool SAMPLED, bool LAZY = false>
 __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int ve, int ebase, float c,
                                           int lane) {
@@ -931,7 +934,59 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   };
 
   // ---- pass 1 ----
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp && p.slot_bytes <= kParallelIssueSlotBytes) {
+    // Small slots (short rows): lane g issues the chunks of consumer group g
+    // (chunk i goes to slot i mod nslots, a multiple of kGroups, so each slot
+    // is refilled by one lane only).  Issuing a copy costs about as much as
+    // moving a few KB, so for small copies independent issuers win (a 1-lane
+    // round of 4 KB rows: 2.95 -> 2.40 us); for large ones one lane issuing in
+    // order lands the first chunks first and is faster.
+    constexpr int nprod = kGroups;
+    if (lane < nprod && ALIGNED && body > 0) {
+      const int nch = (body + slot_elems - 1) / slot_elems;  // chunks per row
+      const uint32_t ns = static_cast<uint32_t>(nslots);
+      int s = lane / nch, ci = lane % nch;  // this lane's first chunk is chunk `lane`
+      uint32_t slot = static_cast<uint32_t>(lane), par = 0;  // lane < nprod <= nslots
+      uint32_t issued = 0;
+      bool ok = true;
+      while (s < nstreams) {
+        const int c0 = ci * slot_elems;
+        const int L = min(slot_elems, body - c0);
+        if (!mbar_wait_bounded(&sh.empty[slot], par ^ 1u)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&sh.full[slot], static_cast<uint32_t>(L * kEsize));
+        bulk_g2s(ring + static_cast<size_t>(slot) * p.slot_bytes,
+                 stream_row(s) + static_cast<int64_t>(v0 + c0) * kEsize, static_cast<uint32_t>(L * kEsize),
+                 &sh.full[slot]);
+        ++issued;
+        ci += nprod;
+        while (ci >= nch) {
+          ci -= nch;
+          ++s;
+        }
+        slot += nprod;
+        if (slot >= ns) {
+          slot -= ns;
+          par ^= 1u;
+        }
+      }
+      // Drain: this lane's last copies (one per slot it owns, newest first)
+      // have landed before shared memory is reused; older ones were waited
+      // on before their slot was refilled.
+      const uint32_t window = ns / static_cast<uint32_t>(nprod);
+      for (uint32_t m = 0; m < issued && m < window; ++m) {
+        if (slot < static_cast<uint32_t>(nprod)) {
+          slot += ns;
+          par ^= 1u;
+        }
+        slot -= nprod;
+        if (!mbar_wait_bounded(&sh.full[slot], par)) ok = false;
+      }
+      if (!ok) atomicOr(&sh.cta_flags, kTimedOut);
+    }
+  } else if (warp == kProducerWarp) {
     if (lane == 0 && ALIGNED) {
       uint32_t it = 0;
       bool ok = true;
