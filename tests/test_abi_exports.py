@@ -104,3 +104,30 @@ def test_binding_constants_match_the_header_defines():
     defines = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(SPEC_\w+)\s+(\d+)u?\b", text)}
     for name in ("SPEC_MAX_DRAFTS", "SPEC_VERIFY_META_BEFORE_WAIT", "SPEC_NGRAM_MAX_MATCH"):
         assert getattr(sv, name) == defines[name], name
+
+
+def test_verify_argument_checks_come_before_any_device_work(lib):
+    """An empty batch, V <= 0, rows < lanes, ld < V, an unknown dtype or a NULL
+    required pointer is rejected on the host, before any CUDA call (so this runs
+    without a GPU; the pointers are never dereferenced)."""
+    fake = 4096  # a non-NULL address the library must not touch
+
+    def args(**kw):
+        a = sv._Args(target_logits=fake, draft_logits=None, dtype=1, ld=64, V=64, lanes=2, rows=4,
+                     draft_tokens=fake, draft_lens=fake, row_offsets=fake, temperatures=fake, seed=1,
+                     committed=fake, out_tokens=fake, lane_status=None, row_stats=None, lane_base=0, flags=0)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+
+    for kw in [dict(lanes=0), dict(lanes=-3), dict(V=0), dict(V=-1), dict(rows=1), dict(ld=63), dict(dtype=7),
+               dict(target_logits=None), dict(draft_tokens=None), dict(draft_lens=None), dict(row_offsets=None),
+               dict(temperatures=None), dict(committed=None), dict(out_tokens=None)]:
+        assert lib.spec_verify_accept(ctypes.byref(args(**kw)), None) == sv.SPEC_ERR_INVALID_ARG, kw
+    out = [ctypes.c_int32() for _ in range(4)]
+    for bad in [(0, 4, 64, 1), (2, 1, 64, 1), (2, 4, 0, 1), (2, 4, 64, 9)]:
+        assert lib.spec_verify_launch_shape(*bad, 0, *[ctypes.byref(o) for o in out]) == sv.SPEC_ERR_INVALID_ARG
+    # an empty commit or uniform request is a no-op, not an error
+    assert lib.spec_round_uniforms(1, 0, 0, 4, None, None) == sv.SPEC_OK
+    assert lib.spec_commit_state(None, None, None, 0, 4, 16, 64, 16, 16, None, None) == sv.SPEC_OK
+    assert lib.spec_commit_state(None, None, None, 3, 0, 16, 64, 16, 16, None, None) == sv.SPEC_ERR_INVALID_ARG

@@ -286,6 +286,16 @@ def test_host_argument_errors():
     assert e.value.code == sv.SPEC_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_vocabulary_of_a_million(dtype):
+    """V = 1,000,003 (odd, past every benchmarked size): 62,504-element slices
+    at 16 CTAs per lane, a ragged tail in every row, greedy and sampled lanes."""
+    r = workloads.make_custom_round(61, DEV, lanes=3, vocab=1_000_003, kmax=5, dtype=dtype, sampled="mixed")
+    orc = run_oracle(r)
+    compare(r, run_gpu(r), orc)
+    compare(r, run_gpu(r, stats=False), orc, check_stats=False)
+
+
 def test_identical_draft_and_target_accepts_everything():
     """q == p: every ratio is 1 > u, so every sampled lane commits k + 1."""
     r = _tiny_round(vocab=5000, k=6, lanes=8, temp=0.8)
