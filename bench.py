@@ -66,7 +66,8 @@ def measured_hbm_peak():
 
 
 # The files the verify and commit kernels are built from (the profiled kernels).
-KERNEL_SOURCES = ["commit_kernel.cuh", "device_ptx.cuh", "philox.cuh", "spec_verify.cu", "verify_kernel.cuh"]
+KERNEL_SOURCES = ["commit_kernel.cuh", "device_ptx.cuh", "philox.cuh", "spec_verify.cu", "verify_kernel.cuh",
+                  "verify_variants.h", "verify_w20.cu", "verify_w20p5.cu"]
 
 
 def kernel_source_hash():

@@ -151,9 +151,12 @@ typedef struct {
  *
  * Launch: one thread-block cluster per lane.  A round with draft_logits runs
  * a build of the kernel with 20 consumer warps per CTA (its sampled lanes are
- * bound by instruction issue), a round without them the 16-warp build; both
- * compute the same results.  The environment variable SPEC_VERIFY_WARPS=16 or
- * 20 forces one build.
+ * bound by instruction issue): in four groups of five when one ring slot holds
+ * a CTA's whole row slice and two slots per group fit, else in five groups of
+ * four.  A round without them runs the 16-warp build.  All compute the same
+ * results (sampled lanes within the stated tolerance of the definition).
+ * SPEC_VERIFY_BUILD=0|1|2 (16 warps; 20 in groups of four; 20 in groups of
+ * five) forces one build.
  *
  * Errors: returns SPEC_ERR_INVALID_ARG for NULL required pointers, V <= 0,
  * lanes <= 0, rows < lanes, ld < V or an unknown dtype; SPEC_ERR_CUDA if the
@@ -220,7 +223,8 @@ const char* spec_status_string(int status);
  *   SPEC_VERIFY_RING_KB=K    ring size in KB (default: all shared memory left)
  *   SPEC_VERIFY_ORDER=0|1    clusters take lanes longest first (default: only when
  *                            the launch has more lanes than resident clusters)
- *   SPEC_VERIFY_WARPS=16|20  which build of the verify kernel runs (see spec_verify_accept)
+ *   SPEC_VERIFY_BUILD=0|1|2  which build of the verify kernel runs (see spec_verify_accept);
+ *                            SPEC_VERIFY_WARPS=16|20 is the same as 0|1
  *   SPEC_COMMIT_CHUNK_KB, SPEC_COMMIT_NBUF, SPEC_COMMIT_CTAS_PER_SM
  *                            copy shape of spec_commit_state (defaults 32, 2, 3)
  * Greedy lanes and the commit give the same results under every override;

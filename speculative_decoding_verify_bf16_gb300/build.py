@@ -3,6 +3,8 @@
 import os
 import shutil
 import subprocess
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 REPO_DIR = os.path.dirname(PKG_DIR)
@@ -14,7 +16,7 @@ LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 NVCC_FLAGS = [
     "-O3", "-std=c++17", "-lineinfo",
     "-gencode", "arch=compute_103a,code=sm_103a",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
 ]
 
 
@@ -48,14 +50,22 @@ def build_library(force=False, verbose=False):
     if not force and up_to_date():
         return LIB_PATH
     tmp = LIB_PATH + ".tmp"
-    cmd = [_nvcc(), *NVCC_FLAGS, "-I" + INCLUDE, "-o", tmp, *_translation_units()]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
-    if verbose:
-        print(res.stdout + res.stderr)
+    nvcc = _nvcc()
+    with tempfile.TemporaryDirectory(prefix="specverify-build-") as objdir:
+        # Translation units compile in parallel (each kernel build is one), then link.
+        units = _translation_units()
+        objs = [os.path.join(objdir, os.path.basename(u) + ".o") for u in units]
+        cmds = [[nvcc, *NVCC_FLAGS, *(["-Xptxas=-v"] if verbose else []), "-I" + INCLUDE, "-c", "-o", o, u]
+                for u, o in zip(units, objs)]
+        with ThreadPoolExecutor(max_workers=max(1, min(len(cmds), os.cpu_count() or 1))) as pool:
+            results = list(pool.map(lambda c: (c, subprocess.run(c, capture_output=True, text=True)), cmds))
+        link = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-o", tmp, *objs]
+        results.append((link, subprocess.run(link, capture_output=True, text=True)))
+        for cmd, res in results:
+            if res.returncode != 0:
+                raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
+            if verbose:
+                print(res.stdout + res.stderr)
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

@@ -18,6 +18,7 @@ namespace {
 using specv::bf16_tag;
 using verify_variants::KernelVariant;
 using verify_variants::w20_variant;
+using verify_variants::w20p5_variant;
 
 constexpr int kMaxDevices = 64;
 
@@ -25,7 +26,7 @@ struct DeviceCache {
   bool ready = false;
   int sms = 0;
   int smem_optin = 0;
-  bool verify_attr[8] = {};  // per kernel build and instantiation
+  bool verify_attr[12] = {};  // per kernel build and instantiation
   bool commit_attr = false;
 };
 
@@ -133,18 +134,25 @@ KernelVariant w16_variant() {
   return v;
 }
 
+// Kernel builds: 0 = 16 consumer warps (4 groups of 4), 1 = 20 warps (5 groups
+// of 4), 2 = 20 warps (4 groups of 5).
+constexpr int kBuildW16 = 0, kBuildW20 = 1, kBuildW20P5 = 2, kBuilds = 3;
+
 // Rounds with drafter logits may hold sampled lanes, whose sweep is bound by
 // instruction issue: 20 consumer warps hide more of its latency.  Greedy-only
-// rounds stream better with 16.  SPEC_VERIFY_WARPS=16|20 overrides.
-int pick_variant(bool with_draft) {
+// rounds stream better with 16.  SPEC_VERIFY_BUILD=0|1|2 (or the older
+// SPEC_VERIFY_WARPS=16|20) forces a build; -1 means "choose by shape".
+int forced_build() {
+  const int b = env_int("SPEC_VERIFY_BUILD", -1);
+  if (b >= 0 && b < kBuilds) return b;
   const int w = env_int("SPEC_VERIFY_WARPS", 0);
-  if (w == 16) return 0;
-  if (w == 20) return 1;
-  return with_draft ? 1 : 0;
+  if (w == 16) return kBuildW16;
+  if (w == 20) return kBuildW20;
+  return -1;
 }
 
 const KernelVariant& variant(int which) {
-  static const KernelVariant kVariants[2] = {w16_variant(), w20_variant()};
+  static const KernelVariant kVariants[kBuilds] = {w16_variant(), w20_variant(), w20p5_variant()};
   return kVariants[which];
 }
 
@@ -249,6 +257,29 @@ int resolve_shape(DeviceCache* dc, int dev, int which, int lanes, int rows, int 
   return SPEC_OK;
 }
 
+// The build and shape a launch uses.  Rounds with drafter logits take the
+// four-groups-of-five build when one slot holds a CTA's whole row slice and
+// the ring holds two slots per group (each group double-buffers); otherwise
+// the five-groups-of-four build, whose ring is a multiple of five slots.
+int resolve_launch(DeviceCache* dc, int dev, bool with_draft, int lanes, int rows, int V, int dtype, bool aligned,
+                   VerifyShape* out, void** kernel_out, int* which_out) {
+  const int forced = forced_build();
+  int which = forced >= 0 ? forced : (with_draft ? kBuildW20P5 : kBuildW16);
+  int rc = resolve_shape(dc, dev, which, lanes, rows, V, dtype, aligned, out, kernel_out);
+  if (forced < 0 && which == kBuildW20P5) {
+    const int esize = (dtype == SPEC_BF16) ? 2 : 4;
+    const bool fits = rc == SPEC_OK && aligned &&
+                      static_cast<int64_t>(out->slice) * esize <= out->slot_bytes &&
+                      out->nslots >= 2 * variant(kBuildW20P5).groups;
+    if (!fits) {
+      which = kBuildW20;
+      rc = resolve_shape(dc, dev, which, lanes, rows, V, dtype, aligned, out, kernel_out);
+    }
+  }
+  *which_out = which;
+  return rc;
+}
+
 }  // namespace
 
 extern "C" {
@@ -298,8 +329,8 @@ int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype 
   int dev = 0;
   if (device_cache(&dc, &dev) != SPEC_OK) return SPEC_ERR_CUDA;
   VerifyShape s{};
-  const int which = pick_variant(with_draft != 0);
-  const int rc = resolve_shape(dc, dev, which, lanes, rows, V, dtype, true, &s, nullptr);
+  int which = 0;
+  const int rc = resolve_launch(dc, dev, with_draft != 0, lanes, rows, V, dtype, true, &s, nullptr, &which);
   if (rc != SPEC_OK) return rc;
   if (cluster_ctas) *cluster_ctas = s.cluster;
   if (threads) *threads = variant(which).threads;
@@ -328,8 +359,9 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
                        ((a->ld * esize) % 16 == 0);
   VerifyShape s{};
   void* kernel = nullptr;
-  const int which = pick_variant(a->draft_logits != nullptr);
-  const int rc = resolve_shape(dc, dev, which, a->lanes, a->rows, a->V, a->dtype, aligned, &s, &kernel);
+  int which = 0;
+  const int rc = resolve_launch(dc, dev, a->draft_logits != nullptr, a->lanes, a->rows, a->V, a->dtype, aligned, &s,
+                                &kernel, &which);
   if (rc != SPEC_OK) return rc;
 
   specv::VerifyParams p{};

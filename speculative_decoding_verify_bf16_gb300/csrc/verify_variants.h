@@ -1,6 +1,6 @@
 // verify_variants.h -- what the host needs to know about one build of the verify
 // kernel (consumer-warp count, threads, shared-memory header, kernel entry
-// points).  Host code only; shared by spec_verify.cu and verify_w20.cu.
+// points).  Host code only; shared by spec_verify.cu and the verify_w20*.cu builds.
 #pragma once
 
 namespace verify_variants {
@@ -13,7 +13,9 @@ struct KernelVariant {
   void* kernel[4] = {nullptr, nullptr, nullptr, nullptr};  // [dtype * 2 + aligned]
 };
 
-// The 20-consumer-warp build (verify_w20.cu).
+// The 20-consumer-warp builds: five groups of four (verify_w20.cu) and four
+// groups of five (verify_w20p5.cu).
 KernelVariant w20_variant();
+KernelVariant w20p5_variant();
 
 }  // namespace verify_variants

@@ -358,22 +358,38 @@ def test_longest_first_lane_order_changes_nothing(monkeypatch, lanes, vocab, kma
 
 
 @pytest.mark.parametrize("sampled,dtype", [("mixed", "bf16"), ("none", "bf16"), ("all", "f32")])
-def test_both_kernel_builds_match_the_oracle(monkeypatch, sampled, dtype):
-    """Rounds with drafter logits run the 20-consumer-warp build of the kernel,
-    rounds without them the 16-warp build.  Forcing either build on either kind
-    of round must match the oracle; greedy lanes are bit-identical between the
-    two (the argmax does not depend on how the warps split the slice)."""
+def test_every_kernel_build_matches_the_oracle(monkeypatch, sampled, dtype):
+    """The kernel is built three times: 16 consumer warps in groups of 4 (rounds
+    without drafter logits), 20 in groups of 4, and 20 in groups of 5 (rounds
+    with them, chosen by shape).  Forcing each build on each kind of round must
+    match the oracle; greedy lanes are bit-identical across builds (the argmax
+    does not depend on how the warps split the slice)."""
     r = workloads.make_custom_round(58, DEV, lanes=11, vocab=50021, kmax=7, dtype=dtype, sampled=sampled)
     orc = run_oracle(r)
     runs = {}
-    for warps in ("16", "20"):
-        monkeypatch.setenv("SPEC_VERIFY_WARPS", warps)
+    for build, warps in (("0", 16), ("1", 20), ("2", 20)):
+        monkeypatch.setenv("SPEC_VERIFY_BUILD", build)
         shape = sv.spec_verify_launch_shape(r.lanes, r.rows, r.vocab, r.target.dtype)
-        assert shape["threads"] == (int(warps) + 2) * 32
-        runs[warps] = run_gpu(r)
-        compare(r, runs[warps], orc)
+        assert shape["threads"] == (warps + 2) * 32
+        runs[build] = run_gpu(r)
+        compare(r, runs[build], orc)
     greedy = r.temperatures.cpu().numpy() <= 0
-    np.testing.assert_array_equal(runs["16"]["committed"][greedy], runs["20"]["committed"][greedy])
+    for build in ("1", "2"):
+        np.testing.assert_array_equal(runs["0"]["committed"][greedy], runs[build]["committed"][greedy])
+
+
+def test_rounds_with_drafter_logits_choose_their_build_by_shape():
+    """Whole-row slices in one slot with two slots per group take the groups-of-5
+    build (the 8-lane sampled round); row slices streamed in several chunks take
+    the groups-of-4 one (the 128-lane ragged round); rounds without drafter
+    logits the 16-warp build.  All three have their threads reported."""
+    s8 = sv.spec_verify_launch_shape(8, 64, 151936, torch.bfloat16, with_draft=True)
+    s128 = sv.spec_verify_launch_shape(128, 563, 262144, torch.bfloat16, with_draft=True)
+    g8 = sv.spec_verify_launch_shape(8, 64, 151936, torch.bfloat16, with_draft=False)
+    assert s8["threads"] == s128["threads"] == 22 * 32 and g8["threads"] == 18 * 32
+    # groups of five: eight 25 KB slots (over 200 KB); groups of four would hold five
+    assert s8["slice"] * 2 <= 40 * 1024 and s8["smem_bytes"] > 8 * s8["slice"] * 2
+    assert s128["slice"] * 2 > 40 * 1024
 
 
 @pytest.mark.parametrize("cluster,ring_kb,slot_kb", [("4", "75", "32"), ("12", "75", "32"), ("16", "88", "32"),
