@@ -1,8 +1,9 @@
 // verify_w20.cu -- the verify kernel built a second time with 20 consumer warps
-// (in its own namespace).  Sampled rows are bound by instruction issue, and the
-// extra warps hide more of their latency; greedy rows stream better with 16.
-// spec_verify.cu launches this build when a round has drafter logits (so it
-// may hold sampled lanes) and the 16-warp build otherwise.
+// in five groups of four (in its own namespace).  Sampled rows are bound by
+// instruction issue, and the extra warps hide more of their latency; greedy
+// rows stream better with 16.  spec_verify.cu launches this build for rounds
+// with drafter logits when the four-groups-of-five build (verify_w20p5.cu)
+// would not double-buffer, and the 16-warp build for rounds without them.
 #define SPEC_VERIFY_CONSUMER_WARPS 20
 #define specv specv_w20
 #include "verify_kernel.cuh"
