@@ -69,6 +69,15 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 #define SPEC_VERIFY_META_BEFORE_WAIT 1u
 
 /*
+ * SPEC_VERIFY_TEST_WITHHOLD_COPY: for tests of the failure path only.  Each
+ * CTA's producer skips its last bulk copy, so the waits for it run out after
+ * the kernel's time limit (2 s) and every lane with rows to stream reports
+ * SPEC_ERR_TIMEOUT (committed 0).  The launch then returns normally and the
+ * context stays usable.  Never set in normal use.
+ */
+#define SPEC_VERIFY_TEST_WITHHOLD_COPY 2u
+
+/*
  * spec_row_budget -- drafts per lane under a row budget.
  *
  * ignis docs, "Speculative decoding" -- "The row budget": a round carries

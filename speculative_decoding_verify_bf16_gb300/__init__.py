@@ -23,6 +23,7 @@ __all__ = [
     "spec_accept_counts_update", "spec_accept_rates_from_counts", "new_accept_counts", "accept_counts_view",
     "spec_backoff_step", "new_backoff_states", "BACKOFF_FIELDS", "ACCEPT_COUNT_WORDS",
     "spec_ngram_draft", "SPEC_NGRAM_MAX_MATCH", "spec_apply_penalties", "SPEC_VERIFY_META_BEFORE_WAIT",
+    "SPEC_VERIFY_TEST_WITHHOLD_COPY",
 ]
 
 SPEC_OK = 0
@@ -35,6 +36,7 @@ SPEC_ERR_LAYOUT = 6
 SPEC_ERR_TIMEOUT = 7
 SPEC_MAX_DRAFTS = 15
 SPEC_VERIFY_META_BEFORE_WAIT = 1
+SPEC_VERIFY_TEST_WITHHOLD_COPY = 2
 
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
@@ -186,7 +188,7 @@ def row_stats_view(buf):
 
 def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, temperatures, seed,
                        committed, out_tokens, lane_status=None, row_stats=None, stream=None,
-                       rows=None, lane_base=0, meta_before_wait=False):
+                       rows=None, lane_base=0, meta_before_wait=False, test_flags=0):
     """Launch the fused verify kernel (see spec_verify_accept in include/spec_verify.h).
 
     target, draft: [rows, >= V] bf16 or float32 CUDA tensors with unit inner
@@ -199,7 +201,8 @@ def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, tem
     split into parts draws the uniforms of the unsplit batch).
     ``meta_before_wait`` sets SPEC_VERIFY_META_BEFORE_WAIT: the caller promises
     that the kernel preceding this launch on the stream did not write
-    draft_tokens, draft_lens, row_offsets or temperatures.
+    draft_tokens, draft_lens, row_offsets or temperatures.  ``test_flags`` adds
+    test-only flags (SPEC_VERIFY_TEST_WITHHOLD_COPY).
     """
     lib = load_library()
     if target.dim() != 2 or target.stride(1) != 1 or target.dtype not in _DTYPES:
@@ -242,7 +245,7 @@ def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, tem
         lane_status=None if lane_status is None else lane_status.data_ptr(),
         row_stats=None if row_stats is None else row_stats.data_ptr(),
         lane_base=int(lane_base),
-        flags=SPEC_VERIFY_META_BEFORE_WAIT if meta_before_wait else 0,
+        flags=(SPEC_VERIFY_META_BEFORE_WAIT if meta_before_wait else 0) | int(test_flags),
     )
     code = lib.spec_verify_accept(ctypes.byref(a), _stream(stream))
     if code != SPEC_OK:

@@ -872,6 +872,9 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   // The lane metadata may be read before the wait for the previous kernel on
   // the stream only when the caller says that kernel did not write it.
   const bool meta_early = (p.flags & SPEC_VERIFY_META_BEFORE_WAIT) != 0u;
+  // Tests only: the producer never issues its last copy, so the waits for it
+  // run out and the lane reports SPEC_ERR_TIMEOUT.
+  const bool withhold_last = (p.flags & SPEC_VERIFY_TEST_WITHHOLD_COPY) != 0u;
   if (!meta_early) griddep_wait();
   if (p.order_by_cost) b = lane_of_rank(p, sh, b);
 
@@ -950,6 +953,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       uint32_t issued = 0;
       bool ok = true;
       while (s < nstreams) {
+        if (withhold_last && s == nstreams - 1 && ci == nch - 1) break;
         const int c0 = ci * slot_elems;
         const int L = min(slot_elems, body - c0);
         if (!mbar_wait_bounded(&sh.empty[slot], par ^ 1u)) {
@@ -993,6 +997,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       for (int s = 0; s < nstreams && ok; ++s) {
         const uint8_t* row = stream_row(s) + static_cast<int64_t>(v0) * kEsize;
         for (int c0 = 0; c0 < body; c0 += slot_elems) {
+          if (withhold_last && s == nstreams - 1 && c0 + slot_elems >= body) break;
           const int L = min(slot_elems, body - c0);
           const uint32_t slot = it % nslots;
           const uint32_t par = (it / nslots) & 1u;

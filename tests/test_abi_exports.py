@@ -102,7 +102,8 @@ def test_binding_structs_match_the_c_layout(struct, cls, tmp_path):
 def test_binding_constants_match_the_header_defines():
     text = "".join(open(p).read() for p in glob.glob(os.path.join(ROOT, "include", "*.h")))
     defines = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(SPEC_\w+)\s+(\d+)u?\b", text)}
-    for name in ("SPEC_MAX_DRAFTS", "SPEC_VERIFY_META_BEFORE_WAIT", "SPEC_NGRAM_MAX_MATCH"):
+    for name in ("SPEC_MAX_DRAFTS", "SPEC_VERIFY_META_BEFORE_WAIT", "SPEC_VERIFY_TEST_WITHHOLD_COPY",
+                 "SPEC_NGRAM_MAX_MATCH"):
         assert getattr(sv, name) == defines[name], name
 
 

@@ -296,6 +296,32 @@ def test_vocabulary_of_a_million(dtype):
     compare(r, run_gpu(r, stats=False), orc, check_stats=False)
 
 
+@pytest.mark.parametrize("vocab", [20000, 200000], ids=["per-group-issue", "single-issuer"])
+@pytest.mark.parametrize("sampled", ["none", "mixed"])
+def test_a_wait_that_never_completes_reports_a_timeout(vocab, sampled):
+    """With SPEC_VERIFY_TEST_WITHHOLD_COPY each CTA's producer skips its last
+    bulk copy: the consumers' wait for it runs out after the kernel's 2 s
+    limit, every lane reports SPEC_ERR_TIMEOUT with nothing committed, the
+    launch returns, and the next launch on the same context matches the oracle."""
+    import time
+
+    r = workloads.make_custom_round(81, DEV, lanes=4, vocab=vocab, kmax=3, dtype="bf16", sampled=sampled,
+                                    fixed_k=True)
+    committed = torch.full((r.lanes,), -7, dtype=torch.int32, device=DEV)
+    out = torch.full((r.rows,), -7, dtype=torch.int32, device=DEV)
+    status = torch.full((r.lanes,), -7, dtype=torch.int32, device=DEV)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    sv.spec_verify_accept(r.target, r.draft, r.draft_tokens, r.draft_lens, r.row_offsets, r.temperatures,
+                          r.seed, committed, out, status, test_flags=sv.SPEC_VERIFY_TEST_WITHHOLD_COPY)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert (status.cpu() == sv.SPEC_ERR_TIMEOUT).all(), status
+    assert (committed.cpu() == 0).all()
+    assert 1.5 < elapsed < 60, elapsed
+    compare(r, run_gpu(r), run_oracle(r))
+
+
 def test_identical_draft_and_target_accepts_everything():
     """q == p: every ratio is 1 > u, so every sampled lane commits k + 1."""
     r = _tiny_round(vocab=5000, k=6, lanes=8, temp=0.8)
