@@ -158,12 +158,14 @@ typedef struct {
  * word 1 gives the draw's u'; u = (word >> 40) * 2^-24.  The draw walks token ids
  * upwards and takes the first whose cumulative weight exceeds u' * W.
  *
- * Launch: one thread-block cluster per lane.  A round with draft_logits runs
- * a build of the kernel with 20 consumer warps per CTA (its sampled lanes are
- * bound by instruction issue): in four groups of five when one ring slot holds
- * a CTA's whole row slice and two slots per group fit, else in five groups of
- * four.  A round without them runs the 16-warp build.  All compute the same
- * results (sampled lanes within the stated tolerance of the definition).
+ * Launch: one thread-block cluster per lane.  When one ring slot holds a
+ * CTA's whole row slice and two slots per group fit, the round runs a build
+ * with 20 consumer warps in four groups of five (each group double-buffers);
+ * a greedy round does so only with slots above 8 KB.  Otherwise a round with
+ * draft_logits runs 20 consumer warps in five groups of four (its sampled
+ * lanes are bound by instruction issue) and a round without them 16 warps.
+ * All compute the same results (sampled lanes within the stated tolerance of
+ * the definition).
  * SPEC_VERIFY_BUILD=0|1|2 (16 warps; 20 in groups of four; 20 in groups of
  * five) forces one build.
  *

@@ -257,22 +257,27 @@ int resolve_shape(DeviceCache* dc, int dev, int which, int lanes, int rows, int 
   return SPEC_OK;
 }
 
-// The build and shape a launch uses.  Rounds with drafter logits take the
-// four-groups-of-five build when one slot holds a CTA's whole row slice and
-// the ring holds two slots per group (each group double-buffers); otherwise
-// the five-groups-of-four build, whose ring is a multiple of five slots.
+// The build and shape a launch uses.  The four-groups-of-five build runs when
+// one slot holds a CTA's whole row slice and the ring holds two slots per group
+// (each group double-buffers): for rounds with drafter logits always then (the
+// 8-lane sampled round 17.6 -> 17.1 us), for greedy rounds only with slots
+// above the parallel-issue size (the 8-lane greedy round 6.33 -> 6.23 us; the
+// 1-lane round of 4 KB rows is faster with 16 warps).  Otherwise rounds with
+// drafter logits take the five-groups-of-four build and greedy rounds the
+// 16-warp one.
 int resolve_launch(DeviceCache* dc, int dev, bool with_draft, int lanes, int rows, int V, int dtype, bool aligned,
                    VerifyShape* out, void** kernel_out, int* which_out) {
   const int forced = forced_build();
-  int which = forced >= 0 ? forced : (with_draft ? kBuildW20P5 : kBuildW16);
+  int which = forced >= 0 ? forced : kBuildW20P5;
   int rc = resolve_shape(dc, dev, which, lanes, rows, V, dtype, aligned, out, kernel_out);
-  if (forced < 0 && which == kBuildW20P5) {
+  if (forced < 0) {
     const int esize = (dtype == SPEC_BF16) ? 2 : 4;
     const bool fits = rc == SPEC_OK && aligned &&
                       static_cast<int64_t>(out->slice) * esize <= out->slot_bytes &&
-                      out->nslots >= 2 * variant(kBuildW20P5).groups;
+                      out->nslots >= 2 * variant(kBuildW20P5).groups &&
+                      (with_draft || out->slot_bytes > specv::kParallelIssueSlotBytes);
     if (!fits) {
-      which = kBuildW20;
+      which = with_draft ? kBuildW20 : kBuildW16;
       rc = resolve_shape(dc, dev, which, lanes, rows, V, dtype, aligned, out, kernel_out);
     }
   }

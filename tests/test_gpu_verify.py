@@ -404,18 +404,24 @@ def test_every_kernel_build_matches_the_oracle(monkeypatch, sampled, dtype):
         np.testing.assert_array_equal(runs["0"]["committed"][greedy], runs[build]["committed"][greedy])
 
 
-def test_rounds_with_drafter_logits_choose_their_build_by_shape():
+def test_rounds_choose_their_kernel_build_by_shape():
     """Whole-row slices in one slot with two slots per group take the groups-of-5
-    build (the 8-lane sampled round); row slices streamed in several chunks take
-    the groups-of-4 one (the 128-lane ragged round); rounds without drafter
-    logits the 16-warp build.  All three have their threads reported."""
+    build: the 8-lane sampled round, and the 8-lane greedy round (its slots are
+    above the parallel-issue size).  Row slices streamed in several chunks take
+    the groups-of-4 build with drafter logits (the 128-lane ragged round) and the
+    16-warp build without (the 64-lane greedy round), as does the 1-lane round of
+    4 KB rows."""
     s8 = sv.spec_verify_launch_shape(8, 64, 151936, torch.bfloat16, with_draft=True)
-    s128 = sv.spec_verify_launch_shape(128, 563, 262144, torch.bfloat16, with_draft=True)
     g8 = sv.spec_verify_launch_shape(8, 64, 151936, torch.bfloat16, with_draft=False)
-    assert s8["threads"] == s128["threads"] == 22 * 32 and g8["threads"] == 18 * 32
+    s128 = sv.spec_verify_launch_shape(128, 563, 262144, torch.bfloat16, with_draft=True)
+    g64 = sv.spec_verify_launch_shape(64, 256, 151936, torch.bfloat16, with_draft=False)
+    g1 = sv.spec_verify_launch_shape(1, 4, 1024, torch.float32, with_draft=False)
+    assert s8["threads"] == g8["threads"] == s128["threads"] == 22 * 32
+    assert g64["threads"] == g1["threads"] == 18 * 32
     # groups of five: eight 25 KB slots (over 200 KB); groups of four would hold five
-    assert s8["slice"] * 2 <= 40 * 1024 and s8["smem_bytes"] > 8 * s8["slice"] * 2
-    assert s128["slice"] * 2 > 40 * 1024
+    for s in (s8, g8):
+        assert s["slice"] * 2 <= 40 * 1024 and s["smem_bytes"] > 8 * s["slice"] * 2
+    assert s128["slice"] * 2 > 40 * 1024 and g64["slice"] * 2 > 40 * 1024
 
 
 @pytest.mark.parametrize("cluster,ring_kb,slot_kb", [("4", "75", "32"), ("12", "75", "32"), ("16", "88", "32"),
