@@ -252,9 +252,9 @@ const char* spec_status_string(int status);
  * V in `dtype` with 16-byte aligned rows on the current device, after the
  * cluster has been shrunk to what the device can schedule (the same rule the
  * launch applies).  `with_draft` != 0 asks for the launch of a round that
- * passes drafter logits: such rounds run a build of the kernel with more
- * consumer warps per CTA (see spec_verify_accept).  Any output pointer may be
- * NULL.  Returns SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED or
+ * passes drafter logits, which can select a different build of the kernel (see
+ * spec_verify_accept; `threads` tells the builds apart).  Any output pointer
+ * may be NULL.  Returns SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED or
  * SPEC_ERR_CUDA.
  */
 int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype dtype, int32_t with_draft,

@@ -5,11 +5,12 @@
 // the k_b + 1 target rows and, on a sampled lane, the k_b drafter rows
 // (ignis docs, "Speculative decoding" -- "One round, step by step", steps 3-4).
 //
-//   pass 1   a producer thread streams the slices through a shared-memory ring
-//            with bulk (TMA) copies; sixteen consumer warps take (chunk, piece)
-//            items and keep, per lane, the running max, the first vector
-//            holding it and, for sampled lanes, the sum of
-//            2^(x * log2(e) / T - fl(max * log2(e) / T))
+//   pass 1   the producer warp streams the slices through a shared-memory
+//            ring with bulk (TMA) copies; 16 or 20 consumer warps (per build)
+//            take (chunk, piece) items and keep, per lane, the running max and
+//            the first vector holding it, and for sampled lanes the sum of
+//            2^(x * log2(e) / T - fl(M * log2(e) / T)) against a reference M
+//            (the running max, or without row_stats any element at or below it)
 //   reduce   greedy rows: one 64-bit key (ordered max, complemented index) per
 //            row, combined with shared-memory atomics and sent to the leader
 //            CTA; sampled rows: per-warp partials merged per CTA and pushed
@@ -17,8 +18,9 @@
 //   scan     the leader (greedy) or every CTA (sampled) runs the lane's
 //            acceptance scan (<= 15 drafts, one lane of warp 0 per position)
 //   pass 2   sampled lanes only: the cluster re-reads one target row (and one
-//            drafter row) from L2, sums the draw weights per slice, exchanges the
-//            sums, and the CTA whose slice holds u' * W walks it to the token
+//            drafter row) from L2, sums the draw weights per round and slice,
+//            exchanges the sums, and the warp whose segment holds u' * W
+//            re-reads the one round that crosses it and walks it to the token
 //
 // Greedy lanes compare raw logits only, so their results are exact.  Sampled
 // lanes use fp32 with the hardware exp2; the acceptance test is done in the
@@ -37,8 +39,8 @@ namespace specv {
 
 constexpr int kMaxDrafts = SPEC_MAX_DRAFTS;      // 15
 constexpr int kMaxStreams = 2 * kMaxDrafts + 1;  // target rows + drafter rows of one lane
-// Consumer warps per CTA.  Sixteen give the latency hiding the sampled rows'
-// exponential sums need; the CTA then occupies a whole SM (one per SM).
+// Consumer warps per CTA (16 by default; the 20-warp builds define it before
+// including this file).  The CTA occupies a whole SM (one per SM).
 #ifndef SPEC_VERIFY_CONSUMER_WARPS
 #define SPEC_VERIFY_CONSUMER_WARPS 16
 #endif

@@ -3,8 +3,9 @@
 // so four groups cover the consumers and the ring needs only a multiple of
 // four slots: when a CTA's whole row slice fits one slot, every group then
 // owns two slots and double-buffers, where the five-group build owns one.
-// spec_verify.cu launches it for rounds with drafter logits whose slices fit
-// that way (the 8-lane sampled round: 17.6 -> 17.1 us).
+// spec_verify.cu launches it for rounds whose slices fit that way: with
+// drafter logits always (the 8-lane sampled round: 17.6 -> 17.1 us), greedy
+// rounds only with slots above 8 KB (the 8-lane greedy round: 6.36 -> 6.3 us).
 #define SPEC_VERIFY_CONSUMER_WARPS 20
 #define SPEC_VERIFY_PIECES 5
 #define specv specv_w20p5
