@@ -79,3 +79,22 @@ def test_the_ragged_workload():
     assert (temps[0::2] <= 0).all()
     assert ((temps[1::2] >= 0.3) & (temps[1::2] <= 1.2)).all() and temps[1::2].std() > 0.15
     assert r.draft is not None and r.draft.shape == r.target.shape
+
+
+def test_state_snapshots_are_finite_distinct_and_reproducible():
+    n = 1 << 16
+    a = workloads.state_block(3, 1, n, seed=9)
+    assert a.dtype == torch.float32 and torch.equal(a, workloads.state_block(3, 1, n, seed=9))
+    mag = a.abs()
+    assert torch.isfinite(a).all() and (mag >= 1).all() and (mag < 2).all()
+    assert 0.45 < (a < 0).float().mean() < 0.55
+    # another lane, column or seed differs in (nearly) every element
+    for other in (workloads.state_block(4, 1, n, seed=9), workloads.state_block(3, 2, n, seed=9),
+                  workloads.state_block(3, 1, n, seed=10)):
+        assert (a == other).float().mean() < 1e-3
+    # element i depends on i: a shifted copy does not match
+    assert (a[1:] == a[:-1]).float().mean() < 1e-3
+    staged, live = workloads.make_state(2, 3, (4, 8), seed=9, device="cpu")
+    assert tuple(staged.shape) == (2, 3, 32) and tuple(live.shape) == (2, 32)
+    assert torch.equal(staged[1, 2], workloads.state_block(1, 2, 32, seed=9))
+    assert torch.equal(live[0], workloads.state_block(0, 3, 32, seed=9))
