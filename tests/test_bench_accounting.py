@@ -1,0 +1,81 @@
+"""bench.py's byte accounting on the CPU: the algorithmic bytes of each
+workload (the rows every round must read, at their element size, plus the
+per-lane metadata and outputs) and the DRAM traffic it takes from the committed
+ncu summaries."""
+
+import numpy as np
+import pytest
+
+import bench
+import workloads
+
+V = 151936
+
+
+def _meta_out(rows, lanes):
+    # draft tokens, lengths, offsets, temperatures; committed, out_tokens, status
+    return 4 * (rows + lanes + (lanes + 1) + lanes) + 4 * (lanes + rows + lanes)
+
+
+def test_greedy_round_reads_every_target_row_once():
+    r = workloads.make_round(workloads.GREEDY_B8, seed=0, device="cpu", with_state=False)
+    total, rows = bench.round_bytes(r)
+    assert rows == 64
+    assert total - _meta_out(64, 8) == 64 * V * 2 == 19_447_808
+
+
+def test_sampled_round_adds_the_drafter_rows():
+    r = workloads.make_round(workloads.SAMPLED_B8, seed=0, device="cpu", with_state=False)
+    total, rows = bench.round_bytes(r)
+    # 8 target rows and 7 drafter rows per lane (the bonus row has no drafter row)
+    assert rows == 64 and total - _meta_out(64, 8) == (64 + 56) * V * 2 == 36_464_640
+
+
+def test_ragged_round_counts_drafter_rows_of_sampled_lanes_only():
+    r = workloads.make_round(workloads.RAGGED_MIXED_B128, seed=0, device="cpu", with_state=False)
+    total, rows = bench.round_bytes(r)
+    k = r.draft_lens.numpy().astype(np.int64)
+    sampled = r.temperatures.numpy() > 0
+    assert rows == int((k + 1).sum()) == r.rows
+    assert total - _meta_out(r.rows, 128) == (r.rows + int(k[sampled].sum())) * 262144 * 2
+
+
+def test_commit_moves_one_snapshot_in_and_out_per_lane():
+    r = workloads.make_round(workloads.GREEDY_COMMIT_B64, seed=0, device="cpu", commit_lanes=1)
+    snapshot = 24 * 16 * 128 * 128 * 4  # fp32 [24][16][128][128]
+    assert snapshot == 25_165_824
+    assert bench.commit_bytes(r) == 2 * snapshot + 8
+    total, rows = bench.round_bytes(r)
+    assert rows == 4 and total - _meta_out(4, 1) == 4 * V * 2
+
+
+def _profile_field(name, field):
+    with open(f"{bench.ROOT}/profiles/{name}") as f:
+        for line in f:
+            if line.startswith(field + ":"):
+                return line.split(":", 1)[1].strip()
+    raise KeyError(field)
+
+
+@pytest.mark.parametrize("kernel,workload,scale", [
+    ("verify_accept", workloads.GREEDY_B8, 1),
+    ("verify_accept", workloads.SAMPLED_B8, 1),
+    ("commit_state", workloads.GREEDY_COMMIT_B64, 4),
+])
+def test_traffic_comes_from_the_summary_of_the_same_kernel_source(kernel, workload, scale, monkeypatch):
+    name = f"{kernel}_{workload}.txt"
+    if _profile_field(name, "kernel_source_sha256") != bench.kernel_source_hash():
+        pytest.skip("the kernel changed since its counters were taken")
+    dram = float(_profile_field(name, "dram_bytes_per_launch"))
+    def mbytes(field):
+        value, unit = _profile_field(name, field).split()
+        return float(value) * {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}[unit]
+    # the per-launch traffic is the read plus the write counter of the capture
+    assert abs(mbytes("dram__bytes_read.sum") + mbytes("dram__bytes_write.sum") - dram) <= 1e3
+    assert bench.profiled_traffic(kernel, workload) == int(dram * scale)
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.profiled_traffic(kernel, workload) is None
+
+
+def test_no_summary_means_no_traffic():
+    assert bench.profiled_traffic("verify_accept", "no_such_workload") is None
