@@ -645,12 +645,15 @@ def run_reference(args):
               if r.target.dtype == torch.bfloat16 else r.target.numpy().astype(np.float64))
     draft = (oracle.decode_bf16(r.draft.view(torch.int16).numpy().view(np.uint16))
              if r.draft is not None else None)
-    # Each step: a bounded sample of the round (whole lanes), sized to ~0.5 s.
+    # Each step: a bounded sample of the round (whole lanes), sized to ~0.5 s
+    # and so that warm-up plus timed steps take about 150 s at most (one lane
+    # a step at least).
+    budget = min(0.5, 150.0 / max(1, args.steps + args.warmup))
     t0 = time.time()
     oracle.verify_round(target, draft, r.draft_tokens.numpy(), r.draft_lens.numpy()[:1], off[:2],
                         r.temperatures.numpy()[:1], seed=r.seed)
     per_lane = max(time.time() - t0, 1e-4)
-    take = int(max(1, min(r.lanes, 0.5 / per_lane)))
+    take = int(max(1, min(r.lanes, budget / per_lane)))
     rows_per_step = int(off[take])
 
     def step():
