@@ -23,3 +23,16 @@ def read_golden(name):
             if line and not line.startswith("#"):
                 rows.append([int(x) for x in line.split()])
     return rows
+
+
+_CPU_ROUNDS = {}
+
+
+def cpu_round(name, seed=0):
+    """A workload generated on the CPU without recurrent state, shared by the
+    CPU tests that only read it (generating the large ones takes seconds)."""
+    key = (name, seed)
+    if key not in _CPU_ROUNDS:
+        import workloads
+        _CPU_ROUNDS[key] = workloads.make_round(name, seed=seed, device="cpu", with_state=False)
+    return _CPU_ROUNDS[key]

@@ -8,6 +8,7 @@ import pytest
 
 import bench
 import workloads
+from conftest import cpu_round
 
 V = 151936
 
@@ -18,21 +19,21 @@ def _meta_out(rows, lanes):
 
 
 def test_greedy_round_reads_every_target_row_once():
-    r = workloads.make_round(workloads.GREEDY_B8, seed=0, device="cpu", with_state=False)
+    r = cpu_round(workloads.GREEDY_B8)
     total, rows = bench.round_bytes(r)
     assert rows == 64
     assert total - _meta_out(64, 8) == 64 * V * 2 == 19_447_808
 
 
 def test_sampled_round_adds_the_drafter_rows():
-    r = workloads.make_round(workloads.SAMPLED_B8, seed=0, device="cpu", with_state=False)
+    r = cpu_round(workloads.SAMPLED_B8)
     total, rows = bench.round_bytes(r)
     # 8 target rows and 7 drafter rows per lane (the bonus row has no drafter row)
     assert rows == 64 and total - _meta_out(64, 8) == (64 + 56) * V * 2 == 36_464_640
 
 
 def test_ragged_round_counts_drafter_rows_of_sampled_lanes_only():
-    r = workloads.make_round(workloads.RAGGED_MIXED_B128, seed=0, device="cpu", with_state=False)
+    r = cpu_round(workloads.RAGGED_MIXED_B128)
     total, rows = bench.round_bytes(r)
     k = r.draft_lens.numpy().astype(np.int64)
     sampled = r.temperatures.numpy() > 0

@@ -6,6 +6,7 @@ import pytest
 import torch
 
 import workloads
+from conftest import cpu_round
 
 
 def _f(t):
@@ -14,12 +15,12 @@ def _f(t):
 
 def _draft_matches_argmax(r):
     """Fraction of drafts d_{j+1} equal to the argmax of row j (greedy lanes)."""
-    x = _f(r.target)
+    best = torch.argmax(r.target.float(), dim=1).numpy()
     off, k = r.row_offsets.numpy(), r.draft_lens.numpy()
     hits = total = 0
     for b in range(r.lanes):
         for j in range(int(k[b])):
-            hits += int(r.draft_tokens[off[b] + j]) == int(np.argmax(x[off[b] + j]))
+            hits += int(r.draft_tokens[off[b] + j]) == int(best[off[b] + j])
             total += 1
     return hits, total
 
@@ -31,7 +32,7 @@ def _draft_matches_argmax(r):
     (workloads.GREEDY_COMMIT_B64, 64, 3, 151936, torch.bfloat16, False),
 ])
 def test_fixed_length_workloads(name, lanes, k, vocab, dtype, sampled):
-    r = workloads.make_round(name, seed=3, device="cpu", with_state=False)
+    r = cpu_round(name, seed=3)
     assert (r.lanes, r.vocab, r.rows) == (lanes, vocab, lanes * (k + 1))
     assert r.target.dtype == dtype and tuple(r.target.shape) == (r.rows, vocab)
     assert (r.draft_lens.numpy() == k).all()
@@ -39,7 +40,7 @@ def test_fixed_length_workloads(name, lanes, k, vocab, dtype, sampled):
     assert (r.draft is not None) == sampled
     temps = r.temperatures.numpy()
     assert (temps == 0.7).all() if sampled else (temps <= 0).all()
-    x = _f(r.target)
+    x = _f(r.target[:32])
     sigma = 3.0 if name == workloads.GREEDY_TINY else 2.0
     # the bulk of each row is N(0, sigma): its middle quantiles
     q25, q75 = np.percentile(x, [25, 75])
@@ -48,9 +49,10 @@ def test_fixed_length_workloads(name, lanes, k, vocab, dtype, sampled):
         # +8 at one token per row lifts the row maxima above those of plain
         # N(0, sigma) rows of the same width (mean 8.8 there, 9.5 here)
         plain = np.random.default_rng(1).standard_normal((64, vocab)) * sigma
-        assert x.max(axis=1).mean() - plain.max(axis=1).mean() > 0.3
+        row_max = r.target.float().amax(dim=1).numpy()
+        assert row_max.mean() - plain.max(axis=1).mean() > 0.3
     if sampled:
-        noise = _f(r.draft) - x
+        noise = _f(r.draft[:32]) - x
         assert abs(noise.std() - 1.0) < 0.05
     else:
         hits, total = _draft_matches_argmax(r)
@@ -68,7 +70,7 @@ def test_the_tiny_workload_matches_drafts_seventy_percent_of_the_time():
 
 
 def test_the_ragged_workload():
-    r = workloads.make_round(workloads.RAGGED_MIXED_B128, seed=5, device="cpu", with_state=False)
+    r = cpu_round(workloads.RAGGED_MIXED_B128, seed=0)
     k = r.draft_lens.numpy()
     off = r.row_offsets.numpy()
     assert r.lanes == 128 and r.vocab == 262144 and r.target.dtype == torch.bfloat16
