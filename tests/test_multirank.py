@@ -1,4 +1,4 @@
-"""Lane sharding across ranks, on CPU with the gloo backend (world size 2).
+"""Lane sharding across ranks, on CPU with the gloo backend (world sizes 2 and 4).
 
 Each rank verifies a contiguous lane range of one round with the CPU oracle,
 using lane_base = its first lane; the gathered results must equal the oracle
@@ -85,10 +85,12 @@ def test_lane_range_partitions():
         lane_range(4, 2, 2)
 
 
-def test_two_gloo_ranks_reproduce_the_unsplit_round(tmp_path):
+@pytest.mark.parametrize("world", [2, 4])
+def test_gloo_ranks_reproduce_the_unsplit_round(tmp_path, world):
+    """9 lanes over 2 ranks (5 + 4) or 4 ranks (3 + 2 + 2 + 2)."""
     import oracle
     out = str(tmp_path / "gathered.pt")
-    mp.spawn(_worker, args=(2, _free_port(), out), nprocs=2, join=True)
+    mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     got = torch.load(out)
     r = _round()
     tgt, drf = _oracle(r)
@@ -96,4 +98,4 @@ def test_two_gloo_ranks_reproduce_the_unsplit_round(tmp_path):
                                r.row_offsets.numpy(), r.temperatures.numpy(), seed=r.seed)
     assert np.array_equal(got["committed"].numpy(), full.committed)
     assert np.array_equal(got["tokens"].numpy(), full.out_tokens)
-    assert got["tmax"] == 2.5
+    assert got["tmax"] == 1.5 + (world - 1)
