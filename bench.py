@@ -17,6 +17,7 @@ maximum over ranks and ``value`` counts the rows of all ranks.
 """
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -358,10 +359,18 @@ def e2e_run(bench, steps, stream):
     return ms, h2d, d2h
 
 
-def cpu_baseline(name, seed, budget_s=12.0):
-    """The oracle as it stands, on a bounded sample of the workload (rank 0 only)."""
+def cpu_baseline(name, seed, budget_s=12.0, gpu_round=None, gpu_out=None):
+    """The oracle as it stands, on a bounded sample of the workload (rank 0 only).
+
+    With ``gpu_round`` (the inputs the GPU verified, copied to the host without
+    any recurrent state) and ``gpu_out`` (its outputs), the oracle runs on
+    those same inputs and the line also counts how many of the sampled lanes'
+    committed counts and tokens equal the GPU's."""
     import oracle
-    r = workloads.make_round(name, seed=seed, device="cpu")
+    if gpu_round is not None:
+        r = dataclasses.replace(gpu_round, staged=None, live=None).to("cpu")
+    else:
+        r = workloads.make_round(name, seed=seed, device="cpu")
     lanes = r.lanes
     off = r.row_offsets.numpy()
     # Sample: as many whole lanes as fit the budget (at least one), from one round.
@@ -387,7 +396,14 @@ def cpu_baseline(name, seed, budget_s=12.0):
             take = max(1, int(take * budget_s / 3 / dt))
     sample = (f"{reps} oracle round(s) over {'all ' if take == lanes else ''}{take} of {lanes} lanes "
               f"({rows_done} rows); bf16 decode of the inputs ({t_dec:.2f} s) excluded")
-    return {"value": rows_done / t_total, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+    out = {"value": rows_done / t_total, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+    if gpu_out is not None:
+        rows = int(off[take])
+        c_gpu = gpu_out["committed"][:take].cpu().numpy()
+        t_gpu = gpu_out["out_tokens"][:rows].cpu().numpy()
+        out["parity"] = {"lanes": take, "committed_equal": int((c_gpu == res.committed).sum()),
+                         "rows": rows, "tokens_equal": int((t_gpu == res.out_tokens).sum())}
+    return out
 
 
 def run_ours(args):
@@ -491,8 +507,20 @@ def run_ours(args):
         "gpu_launches": K * bench.launches_per_step,
         "clocks": clocks,
     }
+    try:
+        committed = bench.outs[0]["committed"].float()
+        line["acceptance"] = {"mean_committed": float(committed.mean()),
+                              "mean_drafts": float(bench.sets[0].draft_lens.float().mean()),
+                              "of": "input set 0, every lane"}
+    except Exception as e:  # a report, never a reason to lose the measurement
+        line["acceptance"] = {"error": repr(e)[:200]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
+        try:
+            line["cpu_baseline"] = cpu_baseline(args.workload, args.seed, gpu_round=bench.sets[0],
+                                                gpu_out=bench.outs[0])
+        except Exception as e:
+            line["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
+            line["cpu_baseline"]["parity"] = {"error": repr(e)[:200]}
     if rank == 0 and args.all_workloads:
         line["workloads"] = other_workloads(args, device, stream, peak)
         line["round_control"] = round_control_timing(device, stream)

@@ -80,3 +80,22 @@ def test_traffic_comes_from_the_summary_of_the_same_kernel_source(kernel, worklo
 
 def test_no_summary_means_no_traffic():
     assert bench.profiled_traffic("verify_accept", "no_such_workload") is None
+
+
+def test_cpu_baseline_counts_parity_on_the_inputs_it_is_given():
+    import oracle
+    import torch
+    r = workloads.make_custom_round(7, "cpu", lanes=6, vocab=500, kmax=5, dtype="bf16", sampled="mixed")
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    full = oracle.verify_round(oracle.decode_bf16(bits(r.target)), oracle.decode_bf16(bits(r.draft)),
+                               r.draft_tokens.numpy(), r.draft_lens.numpy(), r.row_offsets.numpy(),
+                               r.temperatures.numpy(), seed=r.seed)
+    out = {"committed": torch.from_numpy(full.committed.copy()), "out_tokens": torch.from_numpy(full.out_tokens.copy())}
+    line = bench.cpu_baseline("unused", 0, budget_s=0.2, gpu_round=r, gpu_out=out)
+    par = line["parity"]
+    assert line["kind"] == "oracle" and line["cores"] == 1 and line["value"] > 0
+    assert par["committed_equal"] == par["lanes"] >= 1 and par["tokens_equal"] == par["rows"] >= par["lanes"]
+    out["committed"][0] += 1
+    out["out_tokens"][0] = -7
+    par = bench.cpu_baseline("unused", 0, budget_s=0.2, gpu_round=r, gpu_out=out)["parity"]
+    assert par["committed_equal"] == par["lanes"] - 1 and par["tokens_equal"] == par["rows"] - 1
