@@ -6,9 +6,12 @@ Tolerances (derived from the arithmetic; see the design notes):
 * a sampled acceptance decision may differ only where the oracle's float64
   |u - p(d)/q(d)| < 1e-5;
 * a drawn token may differ only if it is still an inverse-CDF draw of the
-  oracle's float64 weights with u' moved by at most 1e-5 + 4e-6 / W
-  (normalised units; W is the residual mass, 1 for a bonus draw): the GPU sums
-  fp32 weights whose absolute errors add up to at most about 2e-6;
+  oracle's float64 weights with u' * W moved by at most 1e-5 * W (W is the
+  total weight of the drawn distribution: the residual mass, or 1 for a draw
+  from p), i.e. where the oracle's draw lay within 1e-5 of a CDF boundary in
+  normalised units;
+* exemptions (acceptance decisions or draws allowed to differ) are counted,
+  and a comparison fails if they exceed 1e-3 of its sampled lanes;
 * log p(d), log q(d) and the log-sum-exp: within 1e-5 (absolute in log space,
   i.e. 1e-5 relative on the probabilities);
 * residual mass: within 1e-5 * W + 2e-6.
@@ -21,11 +24,14 @@ import oracle
 import speculative_decoding_verify_bf16_gb300 as sv
 
 ACCEPT_TOL = 1e-5
+DRAW_TOL = 1e-5
 LOG_TOL = 1e-5
+EXEMPT_FRAC = 1e-3
 
 
-def draw_tol(mass):
-    return 1e-5 + 4e-6 / max(float(mass), 1e-30)
+def exemption_cap(sampled_lanes):
+    """Most exempted decisions one comparison accepts: 1e-3 of its sampled lanes."""
+    return int(EXEMPT_FRAC * sampled_lanes)
 
 
 def logits_to_numpy(t, vocab):
@@ -83,12 +89,12 @@ def draw_is_valid(r, orc, b, n, token, u_draw, target, draft):
     """The GPU's drawn token is an inverse-CDF draw of the oracle's weights, up to tolerance.
 
     Token x is valid iff C(x) - w(x) - tau <= u' * W <= C(x) + tau, with C the
-    float64 cumulative weight and tau = (1e-5 + 4e-6 / W) * W.
+    float64 cumulative weight and tau = 1e-5 * W.
     """
     w = _draw_row_weights(r, orc, b, n, target, draft)
     cdf = np.cumsum(w)
     total = cdf[-1]
-    tau = draw_tol(total) * total
+    tau = DRAW_TOL * total
     t = u_draw * total
     return (cdf[token] - w[token] - tau <= t <= cdf[token] + tau), w[token]
 
@@ -98,8 +104,8 @@ def compare(r, gpu, orc, check_stats=True, oracle_inputs=None):
 
     Greedy lanes, statuses and row statistics must match exactly / to LOG_TOL.
     A sampled lane must match too, except where the oracle shows the decision
-    on which the two differ was within tolerance of flipping.  Returns a dict
-    of counts.
+    on which the two differ was within tolerance of flipping; such exemptions
+    may number at most 1e-3 of the sampled lanes.  Returns a dict of counts.
     """
     off = r.row_offsets.cpu().numpy()
     lens = r.draft_lens.cpu().numpy()
@@ -150,6 +156,8 @@ def compare(r, gpu, orc, check_stats=True, oracle_inputs=None):
             if np.isfinite(orc.resid_mass[lo + n]):
                 w = orc.resid_mass[lo + n]
                 assert abs(gpu["resid_mass"][lo + n] - w) <= 1e-5 * w + 2e-6, (b, gpu["resid_mass"][lo + n], w)
+    exempt = counts["accept_flips"] + counts["draw_flips"]
+    assert exempt <= exemption_cap(counts["sampled"]), ("exemptions above 1e-3 of the sampled lanes", counts)
     return counts
 
 
