@@ -39,7 +39,7 @@ import workloads  # noqa: E402
 METRIC = "verified logit rows/sec and achieved HBM GB/s (% of GB300 peak) per verify round"
 UNIT = "rows/s"
 L2_BYTES = 129 * 2 ** 20
-DEFAULT_WORKLOAD = workloads.GREEDY_B8
+DEFAULT_WORKLOAD = workloads.RAGGED_MIXED_B128  # the largest single-GPU workload
 GRAPH_STEPS = 500          # steps per captured graph
 SOAK_SECONDS = 1.0         # untimed replays before the timed region (clocks settle, samples exist)
 FALLBACK_HBM_GBS = 6800.0  # used only if MEASURED_PEAKS.json is absent
@@ -207,10 +207,25 @@ class Bench:
                                   s.temperatures, s.seed, o["committed"], o["out_tokens"], o["status"],
                                   rows=s.rows, lane_base=rank * s.lanes, meta_before_wait=True)
                      for s, o in zip(self.sets, self.outs)]
-        self.verify_bytes, self.rows_per_step = round_bytes(first)
+        # Ragged workloads draw their draft lengths per seed, so the sets differ
+        # in rows and bytes: K steps count the sets they actually ran.
+        per_set = [round_bytes(s) for s in self.sets]
+        self.set_verify_bytes = [b for b, _ in per_set]
+        self.set_rows = [r.rows for r in self.sets]
+        self.verify_bytes, self.rows_per_step = per_set[0]
         self.has_state = first.staged is not None
         self.commit_bytes = commit_bytes(first) if self.has_state else 0
         self.launches_per_step = 1 + (1 if self.has_state else 0)
+
+    def rows_in(self, steps):
+        """Verified rows over `steps` consecutive steps from step 0."""
+        n = len(self.sets)
+        return sum(self.set_rows[i % n] for i in range(steps))
+
+    def mean_verify_bytes(self, steps):
+        """Algorithmic bytes of one verify launch, averaged over `steps` steps from step 0."""
+        n = len(self.sets)
+        return sum(self.set_verify_bytes[i % n] for i in range(steps)) / steps
 
     def check_budget(self):
         r = self.sets[0]
@@ -283,40 +298,42 @@ def e2e_run(bench, steps, stream):
     Every step copies its whole input set from pinned host memory (the logits
     and one packed buffer of draft tokens, draft lengths, row offsets and
     temperatures) and reads back one packed buffer of committed counts and
-    tokens.  Inputs are double-buffered on the device: a copy stream uploads
-    step i + 1 while step i verifies, so the step is bound by the upload."""
+    tokens.  Two input sets alternate, each with its own device buffers: a
+    copy stream uploads step i + 1 while step i verifies, so the step is bound
+    by the upload.  Returns (ms, rows verified, mean H2D bytes a step, mean D2H
+    bytes a step)."""
     sv = bench.sv
-    s0 = bench.sets[0]
-    lanes, rows = s0.lanes, s0.rows
-    n_meta = rows + lanes + (lanes + 1) + lanes  # draft_tokens | draft_lens | row_offsets | temperatures
+    sets = bench.sets[:2] if len(bench.sets) >= 2 else bench.sets[:1] * 2
 
     def pack_meta(s):
         return torch.cat([s.draft_tokens.cpu(), s.draft_lens.cpu(), s.row_offsets.cpu(),
                           s.temperatures.cpu().view(torch.int32)])
 
-    hosts = []
-    for s in bench.sets[:2]:
+    hosts, devs, shapes = [], [], []
+    for s in sets:
         h = {"target": s.target.cpu().pin_memory(), "meta": pack_meta(s).pin_memory()}
         if s.draft is not None:
             h["draft"] = s.draft.cpu().pin_memory()
         hosts.append(h)
-    devs = [{k: torch.empty_like(v, device=bench.device) for k, v in hosts[0].items()} for _ in range(2)]
+        devs.append({k: torch.empty_like(v, device=bench.device) for k, v in h.items()})
+        shapes.append((s.lanes, s.rows, s.seed))
 
-    def views(d):
-        m = d["meta"]
+    def views(i):
+        lanes, rows, _ = shapes[i]
+        m = devs[i]["meta"]
         return (m[:rows], m[rows:rows + lanes], m[rows + lanes:rows + 2 * lanes + 1],
                 m[rows + 2 * lanes + 1:].view(torch.float32))
 
-    res_dev = [torch.empty(lanes + rows, dtype=torch.int32, device=bench.device) for _ in range(2)]
-    res_host = [torch.empty(lanes + rows, dtype=torch.int32).pin_memory() for _ in range(2)]
-    h2d = sum(v.numel() * v.element_size() for v in hosts[0].values())
-    d2h = res_host[0].numel() * 4
+    res_dev = [torch.empty(sh[0] + sh[1], dtype=torch.int32, device=bench.device) for sh in shapes]
+    res_host = [torch.empty(sh[0] + sh[1], dtype=torch.int32).pin_memory() for sh in shapes]
+    h2d = [sum(v.numel() * v.element_size() for v in h.values()) for h in hosts]
+    d2h = [r.numel() * 4 for r in res_host]
     copy_stream = torch.cuda.Stream(device=bench.device)
     uploaded = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
 
     def upload(i):
-        d, h = devs[i % 2], hosts[i % len(hosts)]
+        d, h = devs[i % 2], hosts[i % 2]
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(consumed[i % 2])  # the verify of step i - 2 has read this buffer
             for k, v in h.items():
@@ -324,15 +341,17 @@ def e2e_run(bench, steps, stream):
             uploaded[i % 2].record(copy_stream)
 
     def verify(i):
-        d = devs[i % 2]
-        stream.wait_event(uploaded[i % 2])
-        dt, dl, ro, te = views(d)
-        r = res_dev[i % 2]
+        j = i % 2
+        d = devs[j]
+        lanes, rows, seed = shapes[j]
+        stream.wait_event(uploaded[j])
+        dt, dl, ro, te = views(j)
+        r = res_dev[j]
         # the metadata comes from the copy stream (behind the event), not from a kernel
-        sv.spec_verify_accept(d["target"], d.get("draft"), dt, dl, ro, te, s0.seed + i, r[:lanes], r[lanes:],
+        sv.spec_verify_accept(d["target"], d.get("draft"), dt, dl, ro, te, seed + i, r[:lanes], r[lanes:],
                               stream=stream, meta_before_wait=True)
-        consumed[i % 2].record(stream)
-        res_host[i % 2].copy_(r, non_blocking=True)
+        consumed[j].record(stream)
+        res_host[j].copy_(r, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for e in consumed:
@@ -355,55 +374,96 @@ def e2e_run(bench, steps, stream):
         torch.cuda.synchronize()
     ms = start.elapsed_time(end)
     # the packed results of the last step equal what the binding wrote
-    assert torch.equal(res_host[(steps - 1) % 2].to(bench.device), res_dev[(steps - 1) % 2])
-    return ms, h2d, d2h
+    last = (steps - 1) % 2
+    assert torch.equal(res_host[last].to(bench.device), res_dev[last])
+    rows = sum(shapes[i % 2][1] for i in range(steps))
+    return ms, rows, sum(h2d[i % 2] for i in range(steps)) / steps, sum(d2h[i % 2] for i in range(steps)) / steps
 
 
-def cpu_baseline(name, seed, budget_s=12.0, gpu_round=None, gpu_out=None):
-    """The oracle as it stands, on a bounded sample of the workload (rank 0 only).
+def cpu_oracle_parity(gpu_round, gpu_out, exempt_tol=1e-5):
+    """The oracle (the C++ statement, on every host thread) on the very inputs
+    the GPU verified (every lane), against the GPU's committed counts and
+    tokens.  A lane counts as equal when both agree; a sampled lane that
+    differs counts as exempt when one of its random decisions lay within 1e-5
+    of flipping in the oracle's float64 arithmetic (|u - p/q|, or u' within
+    1e-5 of a CDF boundary in normalised units), and as a mismatch otherwise."""
+    from oracle import native
+    r = dataclasses.replace(gpu_round, staged=None, live=None).to("cpu")
+    tgt, dft, tok, lens, off, temps = cpu_oracle_inputs(r)
+    res = native.verify_round(tgt, dft, tok, lens, off, temps, seed=r.seed, threads=cpu_threads())
+    c_gpu = gpu_out["committed"].cpu().numpy()
+    t_gpu = gpu_out["out_tokens"].cpu().numpy()
+    out = {"lanes": r.lanes, "greedy_lanes": int((temps <= 0).sum()), "sampled_lanes": int((temps > 0).sum()),
+           "greedy_equal": 0, "sampled_equal": 0, "sampled_exempt": 0, "mismatch": 0,
+           "rows": int(off[-1]), "tokens_equal": int((t_gpu[:off[-1]] == res.out_tokens[:off[-1]]).sum())}
+    for b in range(r.lanes):
+        lo, hi = int(off[b]), int(off[b + 1])
+        same = c_gpu[b] == res.committed[b] and np.array_equal(t_gpu[lo:hi], res.out_tokens[lo:hi])
+        if same:
+            out["sampled_equal" if temps[b] > 0 else "greedy_equal"] += 1
+        elif temps[b] > 0 and any(m < exempt_tol for _, _, m in res.margins[b]):
+            out["sampled_exempt"] += 1
+        else:
+            out["mismatch"] += 1
+    return out
 
-    With ``gpu_round`` (the inputs the GPU verified, copied to the host without
-    any recurrent state) and ``gpu_out`` (its outputs), the oracle runs on
-    those same inputs and the line also counts how many of the sampled lanes'
-    committed counts and tokens equal the GPU's."""
-    import oracle
-    if gpu_round is not None:
-        r = dataclasses.replace(gpu_round, staged=None, live=None).to("cpu")
-    else:
-        r = workloads.make_round(name, seed=seed, device="cpu")
+
+def cpu_oracle_inputs(r):
+    """The arguments of the C++ oracle for round r (on the host): logits as
+    stored (bfloat16 bit patterns or float32, widened exactly by the oracle)."""
+    def raw(t):
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+    return (raw(r.target), None if r.draft is None else raw(r.draft), r.draft_tokens.numpy(),
+            r.draft_lens.numpy(), r.row_offsets.numpy(), r.temperatures.numpy())
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_time_oracle(r, budget_s, threads):
+    """Whole rounds of the C++ oracle (oracle/verify_ref.cpp) on `threads` host
+    threads until `budget_s` is spent; if one round would take more than a
+    third of it, the first lanes only.  Returns (rows/s, threads used, sample)."""
+    from oracle import native
+    tgt, dft, tok, lens, off, temps = cpu_oracle_inputs(r)
     lanes = r.lanes
-    off = r.row_offsets.numpy()
-    # Sample: as many whole lanes as fit the budget (at least one), from one round.
-    t_dec = time.time()
-    target = (oracle.decode_bf16(r.target.view(torch.int16).numpy().view(np.uint16))
-              if r.target.dtype == torch.bfloat16 else r.target.numpy().astype(np.float64))
-    draft = None
-    if r.draft is not None:
-        draft = oracle.decode_bf16(r.draft.view(torch.int16).numpy().view(np.uint16))
-    t_dec = time.time() - t_dec
-    rows_done, t_total, reps = 0, 0.0, 0
     take = lanes
+    rows_done, t_total, reps, used = 0, 0.0, 0, threads
     while t_total < budget_s:
-        t0 = time.time()
-        res = oracle.verify_round(target, draft, r.draft_tokens.numpy(), r.draft_lens.numpy()[:take],
-                                  off[:take + 1], r.temperatures.numpy()[:take], seed=r.seed)
-        dt = time.time() - t0
+        t0 = time.perf_counter()
+        res, used = native.verify_round(tgt, dft, tok[:off[take]], lens[:take], off[:take + 1], temps[:take],
+                                        seed=r.seed, threads=threads, return_threads=True)
+        dt = time.perf_counter() - t0
         assert (res.lane_status == 0).all()
         t_total += dt
         rows_done += int(off[take])
         reps += 1
         if reps == 1 and dt > budget_s / 3 and take > 1:
             take = max(1, int(take * budget_s / 3 / dt))
-    sample = (f"{reps} oracle round(s) over {'all ' if take == lanes else ''}{take} of {lanes} lanes "
-              f"({rows_done} rows); bf16 decode of the inputs ({t_dec:.2f} s) excluded")
-    out = {"value": rows_done / t_total, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
-    if gpu_out is not None:
-        rows = int(off[take])
-        c_gpu = gpu_out["committed"][:take].cpu().numpy()
-        t_gpu = gpu_out["out_tokens"][:rows].cpu().numpy()
-        out["parity"] = {"lanes": take, "committed_equal": int((c_gpu == res.committed).sum()),
-                         "rows": rows, "tokens_equal": int((t_gpu == res.out_tokens).sum())}
-    return out
+    sample = (f"{reps} round(s) over {'all ' if take == lanes else 'the first '}{take} of {lanes} lanes "
+              f"({rows_done} rows)")
+    return rows_done / t_total, used, sample
+
+
+def cpu_baseline(name, seed, budget_s=12.0, gpu_round=None):
+    """The oracle as it stands -- the plain C++ statement, oracle/verify_ref.cpp,
+    with one std::thread worker per host thread taking lanes one at a time --
+    timed on a bounded sample of the workload on this host's cores, plus the
+    same on one thread (rank 0 only).  With ``gpu_round`` (an input set the GPU
+    verified) it is timed on those same inputs."""
+    r = dataclasses.replace(gpu_round if gpu_round is not None else workloads.make_round(
+        name, seed=seed, device="cpu", with_state=False), staged=None, live=None).to("cpu")
+    cores = cpu_threads()
+    value, used, sample = cpu_time_oracle(r, budget_s * 0.5, cores)
+    one, _, one_sample = cpu_time_oracle(r, budget_s * 0.5, 1)
+    return {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+            "impl": "C++ float64 (oracle/verify_ref.cpp), std::thread workers over lanes",
+            "sample": f"{sample} on {used} host threads",
+            "single_thread": {"value": one, "unit": UNIT, "cores": 1, "sample": one_sample}}
 
 
 def run_ours(args):
@@ -445,16 +505,17 @@ def run_ours(args):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     ms_total, ms_verify, ms_commit = t.tolist()
 
-    e2e_ms, h2d, d2h = e2e_run(bench, max(5, min(K, 50)), stream)
     e2e_steps = max(5, min(K, 50))
+    e2e_ms, e2e_rows, h2d, d2h = e2e_run(bench, e2e_steps, stream)
     e2e_t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
     if world > 1:
         torch.distributed.all_reduce(e2e_t, op=torch.distributed.ReduceOp.MAX)
 
     peak, peak_kind = measured_hbm_peak()
     verify_us = ms_verify * 1e3 / K
-    verify_gbs = bench.verify_bytes / (verify_us * 1e-6) / 1e9
-    kernels = {"verify_accept": {"us_per_launch": verify_us, "algorithmic_bytes": bench.verify_bytes,
+    verify_bytes = bench.mean_verify_bytes(K)
+    verify_gbs = verify_bytes / (verify_us * 1e-6) / 1e9
+    kernels = {"verify_accept": {"us_per_launch": verify_us, "algorithmic_bytes": verify_bytes,
                                  "gbs": verify_gbs, "frac_of_peak": verify_gbs / peak}}
     dominant = "verify_accept"
     if bench.has_state:
@@ -466,7 +527,7 @@ def run_ours(args):
             dominant = "commit_state"
     dk = kernels[dominant]
     traffic = profiled_traffic(dominant, args.workload)
-    rows_total = bench.rows_per_step * K * world
+    rows_total = bench.rows_in(K) * world
     value = rows_total / (ms_total * 1e-3)
 
     line = {
@@ -486,7 +547,7 @@ def run_ours(args):
             "workload": args.workload,
             "lanes": bench.sets[0].lanes,
             "vocab": bench.sets[0].vocab,
-            "rows_per_step": bench.rows_per_step,
+            "rows_per_step": bench.rows_in(K) / K,
             "logits_dtype": bench.sets[0].dtype,
             "recurrent_state": bench.has_state,
             "l2": (f"inputs rotate over {len(bench.sets)} sets of {bench.set_bytes / 2**20:.1f} MiB "
@@ -500,10 +561,11 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": dk["algorithmic_bytes"],
                      "us_per_launch": dk["us_per_launch"], "peak_source": peak_kind},
         "kernels": kernels,
-        "e2e": {"value": bench.rows_per_step * e2e_steps * world / (e2e_t.item() * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+        "e2e": {"value": e2e_rows * world / (e2e_t.item() * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "path": ("pinned host inputs -> H2D (logits + one packed metadata buffer, double-buffered on a copy "
-                         "stream) -> spec_verify_accept (python binding) -> D2H of one packed result buffer")},
+                         "stream) -> spec_verify_accept (python binding) -> D2H of one packed result buffer; "
+                         "two input sets alternate")},
         "gpu_launches": K * bench.launches_per_step,
         "clocks": clocks,
     }
@@ -515,11 +577,10 @@ def run_ours(args):
     except Exception as e:  # a report, never a reason to lose the measurement
         line["acceptance"] = {"error": repr(e)[:200]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.seed, gpu_round=bench.sets[0])
         try:
-            line["cpu_baseline"] = cpu_baseline(args.workload, args.seed, gpu_round=bench.sets[0],
-                                                gpu_out=bench.outs[0])
-        except Exception as e:
-            line["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
+            line["cpu_baseline"]["parity"] = cpu_oracle_parity(bench.sets[0], bench.outs[0])
+        except Exception as e:  # a report, never a reason to lose the measurement
             line["cpu_baseline"]["parity"] = {"error": repr(e)[:200]}
     if rank == 0 and args.all_workloads:
         line["workloads"] = other_workloads(args, device, stream, peak)
@@ -642,16 +703,23 @@ def other_workloads(args, device, stream, peak):
         ms, _ = timed_graph_run(b, K, stream, 1)
         ms_v, _ = timed_graph_run(b, K, stream, 1, commit=False)
         v_us = ms_v * 1e3 / K
-        entry = {"rows_per_s": b.rows_per_step * K / (ms * 1e-3), "ms_per_step": ms / K,
-                 "verify_us": v_us, "verify_gbs": b.verify_bytes / (v_us * 1e-6) / 1e9,
-                 "verify_frac": b.verify_bytes / (v_us * 1e-6) / 1e9 / peak,
-                 "verify_algorithmic_bytes": b.verify_bytes, "rows_per_step": b.rows_per_step}
+        vb = b.mean_verify_bytes(K)
+        entry = {"rows_per_s": b.rows_in(K) / (ms * 1e-3), "ms_per_step": ms / K,
+                 "verify_us": v_us, "verify_gbs": vb / (v_us * 1e-6) / 1e9,
+                 "verify_frac": vb / (v_us * 1e-6) / 1e9 / peak,
+                 "verify_algorithmic_bytes": vb, "rows_per_step": b.rows_in(K) / K}
         if b.has_state:
             ms_c, _ = timed_graph_run(b, K, stream, 1, verify=False)
             c_us = ms_c * 1e3 / K
             entry.update({"commit_us": c_us, "commit_gbs": b.commit_bytes / (c_us * 1e-6) / 1e9,
                           "commit_frac": b.commit_bytes / (c_us * 1e-6) / 1e9 / peak,
                           "commit_algorithmic_bytes": b.commit_bytes})
+        if not args.no_cpu_baseline:
+            entry["cpu_baseline"] = cpu_baseline(name, args.seed, budget_s=3.0, gpu_round=b.sets[0])
+            try:
+                entry["cpu_baseline"]["parity"] = cpu_oracle_parity(b.sets[0], b.outs[0])
+            except Exception as e:
+                entry["cpu_baseline"]["parity"] = {"error": repr(e)[:200]}
         out[name] = entry
         del b
         torch.cuda.empty_cache()
@@ -663,39 +731,39 @@ def other_workloads(args, device, stream, peak):
 # ---------------------------------------------------------------------------
 
 def run_reference(args):
+    """The reference arm: the CPU oracle (the plain C++ statement, on every
+    host thread) timed as it stands on the same workload, metric and unit."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    import oracle
-    r = workloads.make_round(args.workload, seed=args.seed, device="cpu")
-    off = r.row_offsets.numpy()
-    target = (oracle.decode_bf16(r.target.view(torch.int16).numpy().view(np.uint16))
-              if r.target.dtype == torch.bfloat16 else r.target.numpy().astype(np.float64))
-    draft = (oracle.decode_bf16(r.draft.view(torch.int16).numpy().view(np.uint16))
-             if r.draft is not None else None)
-    # Each step: a bounded sample of the round (whole lanes), sized to ~0.5 s
-    # and so that warm-up plus timed steps take about 150 s at most (one lane
-    # a step at least).
+    from oracle import native
+    native.build()
+    r = workloads.make_round(args.workload, seed=args.seed, device="cpu", with_state=False)
+    tgt, dft, tok, lens, off, temps = cpu_oracle_inputs(r)
+    threads = cpu_threads()
+    # Each step: a bounded sample of the round (its first lanes), sized to
+    # ~0.5 s and so that warm-up plus timed steps take about 150 s at most
+    # (one lane a step at least).
     budget = min(0.5, 150.0 / max(1, args.steps + args.warmup))
-    t0 = time.time()
-    oracle.verify_round(target, draft, r.draft_tokens.numpy(), r.draft_lens.numpy()[:1], off[:2],
-                        r.temperatures.numpy()[:1], seed=r.seed)
-    per_lane = max(time.time() - t0, 1e-4)
-    take = int(max(1, min(r.lanes, budget / per_lane)))
+    t0 = time.perf_counter()
+    _, used = native.verify_round(tgt, dft, tok, lens, off, temps, seed=r.seed, threads=threads,
+                                  return_threads=True)
+    per_round = max(time.perf_counter() - t0, 1e-6)
+    take = int(max(1, min(r.lanes, r.lanes * budget / per_round)))
     rows_per_step = int(off[take])
 
     def step():
-        return oracle.verify_round(target, draft, r.draft_tokens.numpy(), r.draft_lens.numpy()[:take],
-                                   off[:take + 1], r.temperatures.numpy()[:take], seed=r.seed)
+        return native.verify_round(tgt, dft, tok[:off[take]], lens[:take], off[:take + 1], temps[:take],
+                                   seed=r.seed, threads=threads, return_threads=True)
 
     for _ in range(args.warmup):
         step()
-    t0 = time.time()
+    t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
-    dt = time.time() - t0
+        _, used = step()
+    dt = time.perf_counter() - t0
     value = rows_per_step * args.steps / dt
-    sample = f"{take} of {r.lanes} lanes ({rows_per_step} rows) per step"
+    sample = f"the first {take} of {r.lanes} lanes ({rows_per_step} rows) per step, on {used} host threads"
     line = {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -703,7 +771,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "lanes": r.lanes, "vocab": r.vocab,
                    "sample": sample},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample,
+                         "impl": "C++ float64 (oracle/verify_ref.cpp), std::thread workers over lanes"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

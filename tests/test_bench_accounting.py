@@ -82,20 +82,48 @@ def test_no_summary_means_no_traffic():
     assert bench.profiled_traffic("verify_accept", "no_such_workload") is None
 
 
-def test_cpu_baseline_counts_parity_on_the_inputs_it_is_given():
+def _oracle_outputs(r):
     import oracle
     import torch
-    r = workloads.make_custom_round(7, "cpu", lanes=6, vocab=500, kmax=5, dtype="bf16", sampled="mixed")
     bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
     full = oracle.verify_round(oracle.decode_bf16(bits(r.target)), oracle.decode_bf16(bits(r.draft)),
                                r.draft_tokens.numpy(), r.draft_lens.numpy(), r.row_offsets.numpy(),
                                r.temperatures.numpy(), seed=r.seed)
-    out = {"committed": torch.from_numpy(full.committed.copy()), "out_tokens": torch.from_numpy(full.out_tokens.copy())}
-    line = bench.cpu_baseline("unused", 0, budget_s=0.2, gpu_round=r, gpu_out=out)
-    par = line["parity"]
-    assert line["kind"] == "oracle" and line["cores"] == 1 and line["value"] > 0
-    assert par["committed_equal"] == par["lanes"] >= 1 and par["tokens_equal"] == par["rows"] >= par["lanes"]
-    out["committed"][0] += 1
-    out["out_tokens"][0] = -7
-    par = bench.cpu_baseline("unused", 0, budget_s=0.2, gpu_round=r, gpu_out=out)["parity"]
-    assert par["committed_equal"] == par["lanes"] - 1 and par["tokens_equal"] == par["rows"] - 1
+    return full, {"committed": torch.from_numpy(full.committed.copy()),
+                  "out_tokens": torch.from_numpy(full.out_tokens.copy())}
+
+
+def test_oracle_parity_counts_every_lane_of_the_inputs_it_is_given():
+    r = workloads.make_custom_round(7, "cpu", lanes=6, vocab=500, kmax=5, dtype="bf16", sampled="mixed")
+    full, out = _oracle_outputs(r)
+    par = bench.cpu_oracle_parity(r, out)
+    assert par["lanes"] == 6 and par["mismatch"] == 0 and par["sampled_exempt"] == 0
+    assert par["greedy_equal"] + par["sampled_equal"] == 6
+    assert par["greedy_equal"] == par["greedy_lanes"] and par["sampled_equal"] == par["sampled_lanes"] >= 1
+    assert par["tokens_equal"] == par["rows"]
+    # a greedy lane that differs is a mismatch, never an exemption
+    greedy = int(np.nonzero(r.temperatures.numpy() <= 0)[0][0])
+    out["committed"][greedy] += 1
+    out["out_tokens"][int(r.row_offsets[greedy])] = -7
+    par = bench.cpu_oracle_parity(r, out)
+    assert par["mismatch"] == 1 and par["tokens_equal"] == par["rows"] - 1
+
+
+def test_oracle_parity_exempts_only_sampled_decisions_near_a_flip():
+    """A sampled lane whose acceptance uniform sits within 1e-5 of p/q may
+    differ (exempt); moved away from the boundary the same difference is a
+    mismatch."""
+    r = workloads.make_custom_round(8, "cpu", lanes=4, vocab=300, kmax=3, dtype="bf16", sampled="all",
+                                    fixed_k=True)
+    full, out = _oracle_outputs(r)
+    out["committed"][1] = 1 if int(full.committed[1]) != 1 else 2
+    par = bench.cpu_oracle_parity(r, out, exempt_tol=1e-5)
+    assert par["mismatch"] == 1 and par["sampled_exempt"] == 0
+    par = bench.cpu_oracle_parity(r, out, exempt_tol=2.0)  # every decision "near a flip"
+    assert par["mismatch"] == 0 and par["sampled_exempt"] == 1
+
+
+def test_cpu_baseline_times_a_sample_of_whole_lanes():
+    r = workloads.make_custom_round(7, "cpu", lanes=6, vocab=500, kmax=5, dtype="bf16", sampled="mixed")
+    line = bench.cpu_baseline("unused", 0, budget_s=0.2, gpu_round=r)
+    assert line["kind"] == "oracle" and line["cores"] >= 1 and line["value"] > 0 and line["unit"] == "rows/s"

@@ -25,7 +25,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["unit"] == "rows/s" and d["higher_is_better"] is True
     assert d["metric"].startswith("verified logit rows/sec")
     assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] >= 3 and d["n_gpus"] == 1
-    assert d["config"]["workload"] == "greedy_b8_k7_v151936"
+    assert d["config"]["workload"] == "ragged_mixed_b128_v262144"  # the largest single-GPU workload
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}

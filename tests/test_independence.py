@@ -29,6 +29,15 @@ def test_oracle_imports_neither_the_library_nor_the_input_generators():
         assert not _imports(path) & {PKG, "workloads", "bench"}, path
 
 
+def test_cpp_oracle_includes_only_the_standard_library():
+    """oracle/verify_ref.cpp shares no header with the CUDA library."""
+    import re
+    src = open(os.path.join(ROOT, "oracle", "verify_ref.cpp")).read()
+    includes = re.findall(r'^\s*#\s*include\s*([<"][^>"]+[>"])', src, flags=re.M)
+    assert includes and all(i.startswith("<") for i in includes), includes
+    assert "cuda" not in " ".join(includes).lower() and "spec_" not in src
+
+
 def test_library_and_input_generators_never_import_the_oracle():
     paths = glob.glob(os.path.join(ROOT, PKG, "*.py")) + glob.glob(os.path.join(ROOT, "workloads", "*.py"))
     for path in paths:
