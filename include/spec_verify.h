@@ -137,15 +137,6 @@ typedef struct {
                                    part's first global lane draws exactly the uniforms
                                    of the unsplit batch; 0 otherwise                */
   uint32_t flags;               /* SPEC_VERIFY_* flags above; 0 for none          */
-  /* Optional scratch for the work-list form of the kernel (see
-   * spec_verify_workspace_size): caller-owned device memory, 256-byte aligned,
-   * zero before its first use.  Every launch leaves the counters in it at zero
-   * again (the rest is scratch the next launch overwrites), so one workspace
-   * serves any number of launches; launches sharing one workspace must not
-   * overlap on the GPU (one stream, or ordered by events).  NULL selects the
-   * cluster form, which needs none. */
-  void* workspace;
-  uint64_t workspace_bytes;     /* size of `workspace` in bytes                  */
 } spec_verify_args;
 
 /*
@@ -183,29 +174,6 @@ typedef struct {
  * launch fails.  Per-lane errors go to lane_status (see spec_status).
  */
 int spec_verify_accept(const spec_verify_args* args, void* stream);
-
-/*
- * spec_verify_workspace_size -- scratch bytes spec_verify_accept can use.
- *
- * With a workspace, rounds whose rows are 16-byte aligned and that have at most
- * 2048 lanes run the work-list form of the verify kernel: one CTA per SM claims
- * (row, vocabulary chunk) items from a counter in the workspace, writes each
- * chunk's partial reduction there, and the CTA that completes a lane's last
- * chunk runs that lane's acceptance scan; the residual / bonus draw is split
- * into chunks the same way, so draws overlap the streaming of other lanes.
- * Its results equal the cluster form's (greedy lanes bit for bit, sampled lanes
- * within the stated tolerance of the definition).  Host-only; writes the bytes
- * a launch over `lanes` lanes, `rows` rows and vocabulary V of `dtype` needs
- * (about 2 * rows * V * element size / 512 + 2 KB per lane).  A larger
- * workspace is always fine.  Returns SPEC_OK or SPEC_ERR_INVALID_ARG (bad
- * sizes, NULL `bytes`).
- *
- * A launch given a workspace that is too small or not 256-byte aligned
- * returns SPEC_ERR_INVALID_ARG.  A launch in which a bounded wait gives up
- * reports SPEC_ERR_TIMEOUT for every lane (nothing committed) and still
- * leaves the workspace's counters at zero.
- */
-int spec_verify_workspace_size(int32_t lanes, int32_t rows, int32_t V, spec_dtype dtype, uint64_t* bytes);
 
 /*
  * spec_commit_state -- roll per-lane recurrent state to the committed count.
@@ -268,10 +236,6 @@ const char* spec_status_string(int status);
  *                            the launch has more lanes than resident clusters)
  *   SPEC_VERIFY_BUILD=0|1|2  which build of the verify kernel runs (see spec_verify_accept);
  *                            SPEC_VERIFY_WARPS=16|20 is the same as 0|1
- *   SPEC_VERIFY_FORM=cluster|split  which form runs when a workspace is given
- *                            (default: the one chosen by shape)
- *   SPEC_SPLIT_CHUNK_KB=K, SPEC_SPLIT_GRID=G  pass-1 chunk (8-24 KB) and CTAs of
- *                            the work-list form
  *   SPEC_COMMIT_CHUNK_KB, SPEC_COMMIT_NBUF, SPEC_COMMIT_CTAS_PER_SM
  *                            copy shape of spec_commit_state (defaults 32, 2, 3)
  * Greedy lanes and the commit give the same results under every override;

@@ -23,7 +23,7 @@ __all__ = [
     "spec_accept_counts_update", "spec_accept_rates_from_counts", "new_accept_counts", "accept_counts_view",
     "spec_backoff_step", "new_backoff_states", "BACKOFF_FIELDS", "ACCEPT_COUNT_WORDS",
     "spec_ngram_draft", "SPEC_NGRAM_MAX_MATCH", "spec_apply_penalties", "SPEC_VERIFY_META_BEFORE_WAIT",
-    "SPEC_VERIFY_TEST_WITHHOLD_COPY", "spec_verify_workspace_size", "new_workspace",
+    "SPEC_VERIFY_TEST_WITHHOLD_COPY",
 ]
 
 SPEC_OK = 0
@@ -73,8 +73,6 @@ class _Args(ctypes.Structure):
         ("row_stats", ctypes.c_void_p),
         ("lane_base", ctypes.c_uint32),
         ("flags", ctypes.c_uint32),
-        ("workspace", ctypes.c_void_p),
-        ("workspace_bytes", ctypes.c_uint64),
     ]
 
 
@@ -119,9 +117,6 @@ def load_library():
     lib.spec_round_uniforms.restype = ctypes.c_int
     lib.spec_round_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_void_p, ctypes.c_void_p]
-    lib.spec_verify_workspace_size.restype = ctypes.c_int
-    lib.spec_verify_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
-                                               ctypes.POINTER(ctypes.c_uint64)]
     lib.spec_verify_launch_shape.restype = ctypes.c_int
     lib.spec_verify_launch_shape.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
                                              ctypes.c_int32] + [ctypes.POINTER(ctypes.c_int32)] * 4
@@ -191,24 +186,9 @@ def row_stats_view(buf):
     return out
 
 
-def spec_verify_workspace_size(lanes, rows, V, dtype=torch.bfloat16):
-    """Workspace bytes spec_verify_accept can use for a round of this size."""
-    n = ctypes.c_uint64()
-    code = load_library().spec_verify_workspace_size(int(lanes), int(rows), int(V), _DTYPES[dtype], ctypes.byref(n))
-    if code != SPEC_OK:
-        raise SpecError(code, "spec_verify_workspace_size")
-    return int(n.value)
-
-
-def new_workspace(lanes, rows, V, dtype=torch.bfloat16, device=None):
-    """A zeroed uint8 device tensor large enough to be the workspace of such a round."""
-    device = device or torch.device("cuda", torch.cuda.current_device())
-    return torch.zeros(spec_verify_workspace_size(lanes, rows, V, dtype), dtype=torch.uint8, device=device)
-
-
 def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, temperatures, seed,
                        committed, out_tokens, lane_status=None, row_stats=None, stream=None,
-                       rows=None, lane_base=0, meta_before_wait=False, test_flags=0, workspace=None):
+                       rows=None, lane_base=0, meta_before_wait=False, test_flags=0):
     """Launch the fused verify kernel (see spec_verify_accept in include/spec_verify.h).
 
     target, draft: [rows, >= V] bf16 or float32 CUDA tensors with unit inner
@@ -222,9 +202,7 @@ def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, tem
     ``meta_before_wait`` sets SPEC_VERIFY_META_BEFORE_WAIT: the caller promises
     that the kernel preceding this launch on the stream did not write
     draft_tokens, draft_lens, row_offsets or temperatures.  ``test_flags`` adds
-    test-only flags (SPEC_VERIFY_TEST_WITHHOLD_COPY).  ``workspace`` (a uint8
-    device tensor from new_workspace(), zero before its first use) lets the
-    round run the work-list form of the kernel.
+    test-only flags (SPEC_VERIFY_TEST_WITHHOLD_COPY).
     """
     lib = load_library()
     if target.dim() != 2 or target.stride(1) != 1 or target.dtype not in _DTYPES:
@@ -249,8 +227,6 @@ def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, tem
         _need(lane_status, "lane_status", torch.int32, dev, lanes)
     if row_stats is not None:
         _need(row_stats, "row_stats", torch.int32, dev, nrows * 8)
-    if workspace is not None:
-        _need(workspace, "workspace", torch.uint8, dev)
     a = _Args(
         target_logits=target.data_ptr(),
         draft_logits=None if draft is None else draft.data_ptr(),
@@ -270,8 +246,6 @@ def spec_verify_accept(target, draft, draft_tokens, draft_lens, row_offsets, tem
         row_stats=None if row_stats is None else row_stats.data_ptr(),
         lane_base=int(lane_base),
         flags=(SPEC_VERIFY_META_BEFORE_WAIT if meta_before_wait else 0) | int(test_flags),
-        workspace=None if workspace is None else workspace.data_ptr(),
-        workspace_bytes=0 if workspace is None else workspace.numel(),
     )
     code = lib.spec_verify_accept(ctypes.byref(a), _stream(stream))
     if code != SPEC_OK:
@@ -285,7 +259,7 @@ def spec_verify_accept_raw(args, stream):
 
 def make_args(target, draft, draft_tokens, draft_lens, row_offsets, temperatures, seed,
               committed, out_tokens, lane_status=None, row_stats=None, V=None, rows=None, lane_base=0,
-              meta_before_wait=False, workspace=None):
+              meta_before_wait=False):
     """Build the C argument struct once (for tight loops that call it repeatedly)."""
     return _Args(
         target_logits=target.data_ptr(),
@@ -306,8 +280,6 @@ def make_args(target, draft, draft_tokens, draft_lens, row_offsets, temperatures
         row_stats=None if row_stats is None else row_stats.data_ptr(),
         lane_base=int(lane_base),
         flags=SPEC_VERIFY_META_BEFORE_WAIT if meta_before_wait else 0,
-        workspace=None if workspace is None else workspace.data_ptr(),
-        workspace_bytes=0 if workspace is None else workspace.numel(),
     )
 
 

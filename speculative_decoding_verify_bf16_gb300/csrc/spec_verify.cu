@@ -11,7 +11,6 @@
 #include "commit_kernel.cuh"
 #include "spec_verify.h"
 #include "verify_kernel.cuh"
-#include "verify_split_host.h"
 #include "verify_variants.h"
 
 namespace {
@@ -286,25 +285,9 @@ int resolve_launch(DeviceCache* dc, int dev, bool with_draft, int lanes, int row
   return rc;
 }
 
-// With a workspace, the work-list form runs on every round it takes unless
-// SPEC_VERIFY_FORM=cluster says otherwise.
-bool use_split_form(const spec_verify_args* a, bool aligned) {
-  if (!split_host::eligible(a->lanes, aligned)) return false;
-  const char* f = std::getenv("SPEC_VERIFY_FORM");
-  if (f != nullptr && std::strcmp(f, "cluster") == 0) return false;
-  return true;
-}
-
 }  // namespace
 
 extern "C" {
-
-int spec_verify_workspace_size(int32_t lanes, int32_t rows, int32_t V, spec_dtype dtype, uint64_t* bytes) {
-  if (bytes == nullptr || lanes <= 0 || rows < lanes || V <= 0 || (dtype != SPEC_F32 && dtype != SPEC_BF16))
-    return SPEC_ERR_INVALID_ARG;
-  *bytes = split_host::workspace_bytes(lanes, rows, V, dtype == SPEC_BF16 ? 2 : 4);
-  return SPEC_OK;
-}
 
 int spec_round_uniforms(uint64_t seed, uint32_t lane_base, int32_t lanes, int32_t positions, float* out,
                         void* stream) {
@@ -379,8 +362,6 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
   const bool aligned = is_aligned16(a->target_logits) &&
                        (a->draft_logits == nullptr || is_aligned16(a->draft_logits)) &&
                        ((a->ld * esize) % 16 == 0);
-  if (a->workspace != nullptr && use_split_form(a, aligned))
-    return split_host::launch(a, dev, dc->sms, dc->smem_optin, stream);
   VerifyShape s{};
   void* kernel = nullptr;
   int which = 0;

@@ -42,9 +42,8 @@ def logits_to_numpy(t, vocab):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(r, stats=True, stream=None, meta_before_wait=False, workspace=None):
-    """Verify round r (device tensors) through the binding; numpy results.
-    With ``workspace`` the round runs the work-list form of the kernel."""
+def run_gpu(r, stats=True, stream=None, meta_before_wait=False):
+    """Verify round r (device tensors) through the binding; numpy results."""
     dev = r.target.device
     lanes, rows = r.lanes, r.rows
     committed = torch.full((lanes,), -7, dtype=torch.int32, device=dev)
@@ -55,32 +54,13 @@ def run_gpu(r, stats=True, stream=None, meta_before_wait=False, workspace=None):
     draft = r.draft[:, :r.vocab] if r.draft is not None else None
     sv.spec_verify_accept(target, draft, r.draft_tokens, r.draft_lens, r.row_offsets,
                           r.temperatures, r.seed, committed, out_tokens, status, row_stats,
-                          stream=stream, rows=rows, meta_before_wait=meta_before_wait, workspace=workspace)
+                          stream=stream, rows=rows, meta_before_wait=meta_before_wait)
     torch.cuda.synchronize()
     res = {"committed": committed.cpu().numpy(), "out_tokens": out_tokens.cpu().numpy(),
            "lane_status": status.cpu().numpy()}
     if stats:
         res.update({k: v.cpu().numpy() for k, v in sv.row_stats_view(row_stats).items()})
     return res
-
-
-def workspace_for(r):
-    """A zeroed workspace for round r (the work-list form of the kernel)."""
-    return sv.new_workspace(r.lanes, r.rows, r.vocab, r.target.dtype, r.target.device)
-
-
-def workspace_counters(ws, lanes):
-    """The parts of a workspace that must be zero when a launch starts: the
-    256-byte header of shared counters, then the per-lane pass-1 and pass-2
-    counters and, after the draw queue, its ready flags (the order and 256-byte
-    alignment of the work-list kernel's workspace layout)."""
-    align = lambda x: (x + 255) // 256 * 256
-    cnt1 = 256
-    cnt2 = align(cnt1 + 4 * lanes)
-    queue = align(cnt2 + 4 * lanes)
-    ready = align(queue + 8 * lanes)
-    end = align(ready + 8 * lanes)
-    return torch.cat([ws[:queue], ws[ready:end]])
 
 
 def run_oracle(r):

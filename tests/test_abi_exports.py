@@ -132,17 +132,3 @@ def test_verify_argument_checks_come_before_any_device_work(lib):
     assert lib.spec_round_uniforms(1, 0, 0, 4, None, None) == sv.SPEC_OK
     assert lib.spec_commit_state(None, None, None, 0, 4, 16, 64, 16, 16, None, None) == sv.SPEC_OK
     assert lib.spec_commit_state(None, None, None, 3, 0, 16, 64, 16, 16, None, None) == sv.SPEC_ERR_INVALID_ARG
-
-
-def test_workspace_size_grows_with_the_round(lib):
-    """The work-list form's scratch: a few MB for the largest benchmarked round,
-    growing with rows, vocabulary and element size; bad sizes are refused."""
-    import torch
-    ragged = sv.spec_verify_workspace_size(128, 1024, 262144, torch.bfloat16)
-    assert 256 * 1024 < ragged < 8 * 2 ** 20
-    assert sv.spec_verify_workspace_size(128, 2048, 262144) > ragged
-    assert sv.spec_verify_workspace_size(128, 1024, 262144, torch.float32) > ragged
-    assert sv.spec_verify_workspace_size(1, 4, 1024, torch.float32) % 256 == 0
-    for bad in [(0, 4, 1024), (4, 3, 1024), (4, 8, 0)]:
-        with pytest.raises(sv.SpecError):
-            sv.spec_verify_workspace_size(*bad)
