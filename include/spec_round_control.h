@@ -150,7 +150,10 @@ int spec_ngram_draft(const int32_t* tokens, const int64_t* hist_offsets, int32_t
  * spec_apply_penalties -- per-row presence and frequency penalties on the
  * target logits of a round (FreeToken tracking issue #828, "PRs": #836 verifies
  * on the target side with per-row presence and frequency penalties), applied
- * in place, on the same stream, right before spec_verify_accept.
+ * on the same stream right before spec_verify_accept.
+ *
+ * THE CALLER'S TARGET LOGITS ARE OVERWRITTEN: the penalised values replace
+ * the stored ones in place (keep a copy if the raw logits are needed again).
  *
  * Row j of lane b scores the position after the anchor and d_1..d_j, so token
  * t's count in that row is c = (its count in the lane's history) + (its count
@@ -158,8 +161,7 @@ int spec_ngram_draft(const int32_t* tokens, const int64_t* hist_offsets, int32_t
  *     z = x - (frequency[b] * c + presence[b])
  * in fp32 with the roundings in that order (product, sum, difference); a bf16
  * logit is then rounded to the nearest bf16 (ties to even) and stored back.
- * Other tokens, the drafter's logits and lanes whose row_offsets disagree with
- * draft_lens (spec_verify_accept reports those) are not touched.
+ * Other tokens and the drafter's logits are not touched.
  *
  * target_logits, dtype, ld, V, lanes, row_offsets, draft_tokens and
  * draft_lens are those of the round's spec_verify_args.  Lane b's history
@@ -168,6 +170,15 @@ int spec_ngram_draft(const int32_t* tokens, const int64_t* hist_offsets, int32_t
  * are ignored.  presence and frequency are per lane (may be NULL: 0).  One CTA
  * per lane; touches (history + drafts) x (k_b + 1) logits of the lane.
  *
+ * lane_status (out [lanes], may be NULL) gets, per lane: SPEC_OK (penalties
+ * applied); SPEC_ERR_INVALID_ARG if the lane's history list is not strictly
+ * ascending (a repeated or out-of-order id) or holds a count < 1;
+ * SPEC_ERR_LAYOUT if row_offsets disagree with draft_lens; SPEC_ERR_UNSUPPORTED
+ * if k_b > SPEC_MAX_DRAFTS.  A lane with any of these keeps its logits
+ * unchanged.  The list is checked on the device before any logit of the lane
+ * is written.  Use a buffer other than the verify's lane_status (the verify
+ * writes every lane's status), or read it before the verify runs.
+ *
  * Errors: SPEC_ERR_INVALID_ARG for NULL target_logits / row_offsets /
  * draft_tokens / draft_lens / pen_* with lanes > 0, lanes < 0, V <= 0, ld < V
  * or an unknown dtype; SPEC_ERR_CUDA if the launch fails.
@@ -175,7 +186,7 @@ int spec_ngram_draft(const int32_t* tokens, const int64_t* hist_offsets, int32_t
 int spec_apply_penalties(void* target_logits, spec_dtype dtype, int64_t ld, int32_t V, int32_t lanes,
                          const int32_t* row_offsets, const int32_t* draft_tokens, const int32_t* draft_lens,
                          const int32_t* pen_tokens, const int32_t* pen_counts, const int64_t* pen_offsets,
-                         const float* presence, const float* frequency, void* stream);
+                         const float* presence, const float* frequency, int32_t* lane_status, void* stream);
 
 #ifdef __cplusplus
 }

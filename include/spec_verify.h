@@ -191,7 +191,9 @@ int spec_verify_accept(const spec_verify_args* args, void* stream);
  * outside 1..cols, or whose lane_status is already non-zero, keeps its live
  * state; the former gets SPEC_ERR_LAYOUT in lane_status.  staged and live must
  * not overlap.  16-byte aligned pointers, strides and sizes use bulk copies;
- * other layouts take a byte-wise path.
+ * other layouts take a byte-wise path.  If a copy does not complete within the
+ * kernel's wait limit (2 s), every lane whose snapshot was not fully copied
+ * gets SPEC_ERR_TIMEOUT; such a lane's live state may be partly written.
  *
  * `lane_status` (may be NULL) is read and updated in place, so passing the
  * verify's lane_status skips lanes that failed there.  Launched after
@@ -238,6 +240,9 @@ const char* spec_status_string(int status);
  *                            SPEC_VERIFY_WARPS=16|20 is the same as 0|1
  *   SPEC_COMMIT_CHUNK_KB, SPEC_COMMIT_NBUF, SPEC_COMMIT_CTAS_PER_SM
  *                            copy shape of spec_commit_state (defaults 32, 2, 3)
+ *   SPEC_COMMIT_TEST_WITHHOLD_COPY=1  tests of the failure path only: the
+ *                            commit's first CTA never issues its first load, so
+ *                            its wait gives up after 2 s (see spec_commit_state)
  * Greedy lanes and the commit give the same results under every override;
  * sampled lanes stay within the stated tolerance of the definition (their
  * fp32 sums are added in an order that follows the shape).

@@ -132,7 +132,7 @@ def load_library():
                                      ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
     lib.spec_apply_penalties.restype = ctypes.c_int
     lib.spec_apply_penalties.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32] + \
-        [ctypes.c_void_p] * 9
+        [ctypes.c_void_p] * 10
     lib.spec_backoff_step.restype = ctypes.c_int
     lib.spec_backoff_step.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
@@ -432,12 +432,15 @@ def spec_ngram_draft(tokens, hist_offsets, k, drafts, draft_lens, match_min=1, m
 
 
 def spec_apply_penalties(target, row_offsets, draft_tokens, draft_lens, pen_tokens, pen_counts, pen_offsets,
-                         presence=None, frequency=None, stream=None):
-    """Per-row presence / frequency penalties on the target logits, in place
-    (see spec_apply_penalties in include/spec_round_control.h).  target: the
-    round's [rows, >= V] bf16/float32 logits (V = target.shape[1], ld its row
-    stride); pen_tokens / pen_counts int32 [n] (per lane ascending distinct ids),
-    pen_offsets int64 [lanes + 1]; presence / frequency float32 [lanes] or None."""
+                         presence=None, frequency=None, lane_status=None, stream=None):
+    """Per-row presence / frequency penalties on the target logits (see
+    spec_apply_penalties in include/spec_round_control.h).  The logits in
+    ``target`` are overwritten with the penalised values.  target: the round's
+    [rows, >= V] bf16/float32 logits (V = target.shape[1], ld its row stride);
+    pen_tokens / pen_counts int32 [n] (per lane ascending distinct ids, counts
+    >= 1), pen_offsets int64 [lanes + 1]; presence / frequency float32 [lanes]
+    or None; lane_status int32 [lanes] or None receives each lane's status (a
+    lane whose list breaks the contract is left untouched)."""
     lib = load_library()
     if target.dim() != 2 or target.stride(1) != 1 or target.dtype not in _DTYPES:
         raise ValueError("target must be a 2-D bf16/float32 tensor with unit inner stride")
@@ -452,9 +455,11 @@ def spec_apply_penalties(target, row_offsets, draft_tokens, draft_lens, pen_toke
     for t, name in ((presence, "presence"), (frequency, "frequency")):
         if t is not None:
             _need(t, name, torch.float32, dev, lanes)
+    if lane_status is not None:
+        _need(lane_status, "lane_status", torch.int32, dev, lanes)
     rc = lib.spec_apply_penalties(_ptr(target), _DTYPES[target.dtype], target.stride(0), target.shape[1], lanes,
                                   _ptr(row_offsets), _ptr(draft_tokens), _ptr(draft_lens), _ptr(pen_tokens),
                                   _ptr(pen_counts), _ptr(pen_offsets), _ptr(presence), _ptr(frequency),
-                                  _stream(stream))
+                                  _ptr(lane_status), _stream(stream))
     if rc != SPEC_OK:
         raise SpecError(rc, "spec_apply_penalties")

@@ -38,6 +38,7 @@ struct CommitParams {
   uint64_t chunks_per_lane;
   uint64_t total_items;    // lanes * chunks_per_lane
   int32_t nbuf;
+  int32_t test_withhold;   // tests only: CTA 0 announces its first load but never issues it
 };
 
 // Committed column of lane b, or -1 if the lane must keep its live state.
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(kCommitThreads) commit_bulk_kernel(const Commi
         pend_size[slot] = size;
         pend_lane[slot] = b;
         mbar_arrive_expect_tx(&bars[slot], size);
+        if (p.test_withhold && blockIdx.x == 0 && item == 0) return true;  // tests only: never copied
         bulk_g2s_hint(bufs + static_cast<size_t>(slot) * p.chunk_bytes, src, size, &bars[slot], pol);
         return true;
       }
@@ -104,9 +106,10 @@ __global__ void __launch_bounds__(kCommitThreads) commit_bulk_kernel(const Commi
       ++inflight;
     }
     int slot = 0;
+    bool timed_out = false;
     while (inflight > 0) {
       if (!mbar_wait_bounded(&bars[slot], (parity >> slot) & 1u)) {
-        if (p.lane_status) p.lane_status[pend_lane[slot]] = SPEC_ERR_TIMEOUT;
+        timed_out = true;
         break;
       }
       parity ^= 1u << slot;
@@ -117,10 +120,20 @@ __global__ void __launch_bounds__(kCommitThreads) commit_bulk_kernel(const Commi
       if (issue(slot)) ++inflight;
       slot = (slot + 1 == p.nbuf) ? 0 : slot + 1;
     }
-    // After a time-out, let every load still in flight land before exiting.
-    for (int i = 0; i < inflight; ++i) {
-      mbar_wait_bounded(&bars[slot], (parity >> slot) & 1u);
-      slot = (slot + 1 == p.nbuf) ? 0 : slot + 1;
+    if (timed_out) {
+      // A load never landed: every lane this CTA still had work for -- the
+      // lanes of the loads in flight and of every item it has not issued --
+      // reports SPEC_ERR_TIMEOUT (its live state may be partly written); the
+      // loads in flight land before the CTA exits.
+      for (int i = 0; i < inflight; ++i) {
+        if (p.lane_status) p.lane_status[pend_lane[slot]] = SPEC_ERR_TIMEOUT;
+        mbar_wait_bounded(&bars[slot], (parity >> slot) & 1u);
+        slot = (slot + 1 == p.nbuf) ? 0 : slot + 1;
+      }
+      for (; next < p.total_items; next += gridDim.x) {
+        const int b = static_cast<int>(next / p.chunks_per_lane);
+        if (p.lane_status && commit_column(p, b) >= 0) p.lane_status[b] = SPEC_ERR_TIMEOUT;
+      }
     }
     bulk_wait_group<0>();
   }

@@ -59,15 +59,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits for the phase of `bar` with the given parity; false on time-out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Waits for the phase of `bar` with the given parity; false after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
   }
 }
+
+// The waits for data pushed by the other CTAs of a cluster (row partials, draw
+// sums) give up only after four times the limit of any single wait: every CTA
+// pushes its data exactly once, even after one of its own waits gave up (then
+// flagged as timed out), so a receiver never exits while a peer that is still
+// within its own limits may write into its shared memory.
+constexpr uint64_t kExchangeWaitLimitNs = 4 * kWaitLimitNs;
 
 // ---------------------------------------------------------------------------
 // Bulk copies (the TMA unit's non-tensor form): contiguous bytes, 16-byte

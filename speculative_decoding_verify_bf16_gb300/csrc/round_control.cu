@@ -174,7 +174,10 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_draft_kernel(const int32_
 // among d_1..d_j.  Threads take (row, history entry) pairs of all the lane's
 // rows at once, and (row, draft) pairs for the first occurrence of each draft
 // d_1..d_j that is not in the (sorted) history list, so every logit is read and
-// written by one thread, once.
+// written by one thread, once.  The history list is checked first (strictly
+// ascending ids, counts >= 1): a lane that breaks it is left untouched and
+// reported, since two entries of one id would have two threads update one
+// logit and an unsorted list would defeat the search for drafts.
 template <bool BF16>
 __global__ void __launch_bounds__(256) apply_penalties_kernel(uint8_t* target, int64_t ld_bytes, int32_t V,
                                                               const int32_t* row_offsets,
@@ -182,12 +185,20 @@ __global__ void __launch_bounds__(256) apply_penalties_kernel(uint8_t* target, i
                                                               const int32_t* draft_lens, const int32_t* pen_tokens,
                                                               const int32_t* pen_counts,
                                                               const int64_t* pen_offsets, const float* presence,
-                                                              const float* frequency) {
+                                                              const float* frequency, int32_t* lane_status) {
   const int b = blockIdx.x;
   const int k = draft_lens[b];
   const int off = row_offsets[b];
-  if (k < 0 || k > SPEC_MAX_DRAFTS || row_offsets[b + 1] - off != k + 1) return;
   const int64_t h0 = pen_offsets[b], h1 = pen_offsets[b + 1];
+  int status = SPEC_OK;
+  if (k < 0 || off < 0 || row_offsets[b + 1] - off != k + 1) status = SPEC_ERR_LAYOUT;
+  else if (k > SPEC_MAX_DRAFTS) status = SPEC_ERR_UNSUPPORTED;
+  bool bad = h1 < h0;
+  for (int64_t e = h0 + threadIdx.x; !bad && e < h1; e += blockDim.x)
+    bad = pen_counts[e] < 1 || (e > h0 && pen_tokens[e] <= pen_tokens[e - 1]);
+  if (__syncthreads_or(bad) && status == SPEC_OK) status = SPEC_ERR_INVALID_ARG;
+  if (threadIdx.x == 0 && lane_status != nullptr) lane_status[b] = status;
+  if (status != SPEC_OK) return;
   const float pres = presence ? presence[b] : 0.f;
   const float freq = frequency ? frequency[b] : 0.f;
   int d[SPEC_MAX_DRAFTS];
@@ -349,7 +360,7 @@ int spec_ngram_draft(const int32_t* tokens, const int64_t* hist_offsets, int32_t
 int spec_apply_penalties(void* target_logits, spec_dtype dtype, int64_t ld, int32_t V, int32_t lanes,
                          const int32_t* row_offsets, const int32_t* draft_tokens, const int32_t* draft_lens,
                          const int32_t* pen_tokens, const int32_t* pen_counts, const int64_t* pen_offsets,
-                         const float* presence, const float* frequency, void* stream) {
+                         const float* presence, const float* frequency, int32_t* lane_status, void* stream) {
   if (lanes < 0 || V <= 0 || ld < V || (dtype != SPEC_F32 && dtype != SPEC_BF16)) return SPEC_ERR_INVALID_ARG;
   if (lanes == 0) return SPEC_OK;
   if (target_logits == nullptr || row_offsets == nullptr || draft_tokens == nullptr || draft_lens == nullptr ||
@@ -359,10 +370,12 @@ int spec_apply_penalties(void* target_logits, spec_dtype dtype, int64_t ld, int3
   uint8_t* t = static_cast<uint8_t*>(target_logits);
   if (dtype == SPEC_BF16) {
     apply_penalties_kernel<true><<<lanes, 256, 0, st>>>(t, ld * 2, V, row_offsets, draft_tokens, draft_lens,
-                                                        pen_tokens, pen_counts, pen_offsets, presence, frequency);
+                                                        pen_tokens, pen_counts, pen_offsets, presence, frequency,
+                                                        lane_status);
   } else {
     apply_penalties_kernel<false><<<lanes, 256, 0, st>>>(t, ld * 4, V, row_offsets, draft_tokens, draft_lens,
-                                                         pen_tokens, pen_counts, pen_offsets, presence, frequency);
+                                                         pen_tokens, pen_counts, pen_offsets, presence, frequency,
+                                                         lane_status);
   }
   return launch_status();
 }

@@ -444,6 +444,7 @@ int spec_commit_state(const void* staged, void* live, const int32_t* committed, 
   p.staged_lane_stride = staged_lane_stride;
   p.staged_col_stride = staged_col_stride;
   p.live_lane_stride = live_lane_stride;
+  p.test_withhold = env_int("SPEC_COMMIT_TEST_WITHHOLD_COPY", 0) != 0;
 
   const bool aligned = is_aligned16(staged) && is_aligned16(live) && bytes_per_col % 16 == 0 &&
                        staged_lane_stride % 16 == 0 && staged_col_stride % 16 == 0 &&

@@ -1154,7 +1154,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       }
       return;
     }
-    const bool waited = mbar_wait_bounded(&sh.xbar, 0);
+    const bool waited = mbar_wait_bounded(&sh.xbar, 0, kExchangeWaitLimitNs);
     unsigned long long key = 0ull;
     uint32_t flags = fl | (waited ? 0u : kTimedOut);
     if (lane < nstreams) {
@@ -1183,7 +1183,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   push_partials(sh, nstreams, C, rank, sh.cta_flags);
 
   // ---- the lane's totals ----
-  if (tid == 0 && !mbar_wait_bounded(&sh.xbar, 0)) atomicOr(&sh.cta_flags, kTimedOut);
+  if (tid == 0 && !mbar_wait_bounded(&sh.xbar, 0, kExchangeWaitLimitNs)) atomicOr(&sh.cta_flags, kTimedOut);
   __syncthreads();
   if (warp < kConsumerWarps) {
     for (int s = warp; s < nstreams; s += kConsumerWarps) {
@@ -1422,7 +1422,15 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
                     0u, 0u, cluster_map(&sh.dbar[buf], tid));
       }
     }
-    if (tid == 0 && !mbar_wait_bounded(&sh.dbar[buf], 0)) atomicOr(&sh.cta_flags, kTimedOut);
+    if (tid == 0 && !mbar_wait_bounded(&sh.dbar[buf], 0, kExchangeWaitLimitNs)) {
+      // A peer's draw sum never came: the lane's outputs (already written as
+      // OK by the leader) cannot be trusted.
+      atomicOr(&sh.cta_flags, kTimedOut);
+      if (leader) {
+        p.committed[b] = 0;
+        if (p.lane_status) p.lane_status[b] = SPEC_ERR_TIMEOUT;
+      }
+    }
     __syncthreads();
 
     W = 0.f;

@@ -106,3 +106,40 @@ def test_commit_workload_full_size():
     for b in (0, 31, 63):
         want = workloads.state_block(b, int(c[b]) - 1, elems, 7, "cpu")
         assert torch.equal(r.live[b].cpu(), want), b
+
+
+def test_a_load_that_never_lands_fails_every_lane_it_leaves_unfinished(monkeypatch):
+    """SPEC_COMMIT_TEST_WITHHOLD_COPY: the commit's first CTA announces its
+    first load but never issues it.  Its wait gives up after 2 s; every lane
+    that CTA still had loads in flight or work left for reports
+    SPEC_ERR_TIMEOUT, and no lane reports OK without its full snapshot in
+    live state.  A plain commit afterwards is exact again."""
+    import time
+
+    lanes, cols, elems = 12, 4, 3 * 2 ** 15  # 384 KB a snapshot: several chunks a lane
+    g = torch.Generator(device=DEV)
+    g.manual_seed(5)
+    staged = torch.randn(lanes, cols, elems, generator=g, device=DEV)
+    live = torch.randn(lanes, elems, generator=g, device=DEV)
+    committed = torch.tensor([1, 2, 3, 4] * 3, dtype=torch.int32, device=DEV)
+    status = torch.zeros(lanes, dtype=torch.int32, device=DEV)
+    live0 = live.clone()
+    monkeypatch.setenv("SPEC_COMMIT_TEST_WITHHOLD_COPY", "1")
+    torch.cuda.synchronize()
+    t0 = time.time()
+    sv.spec_commit_state(staged, live, committed, status)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    st = status.cpu().numpy()
+    assert 1.5 < elapsed < 60, elapsed
+    assert set(st.tolist()) <= {sv.SPEC_OK, sv.SPEC_ERR_TIMEOUT} and (st == sv.SPEC_ERR_TIMEOUT).any(), st
+    c = committed.cpu().numpy()
+    for b in range(lanes):
+        if st[b] == sv.SPEC_OK:
+            assert torch.equal(live[b], staged[b, c[b] - 1]), b
+    monkeypatch.delenv("SPEC_COMMIT_TEST_WITHHOLD_COPY")
+    status.zero_()
+    live.copy_(live0)
+    sv.spec_commit_state(staged, live, committed, status)
+    torch.cuda.synchronize()
+    _check(staged, live0, live, c, np.zeros(lanes, np.int32), status.cpu().numpy())

@@ -241,13 +241,61 @@ def test_penalties_match_the_oracle_and_feed_the_verify(dtype, sampled, seed):
     compare(r, run_gpu(r), run_oracle(r))
 
 
+def test_penalty_lists_that_break_the_contract_are_reported_and_left_alone():
+    """The history list of a lane must hold distinct ids in ascending order with
+    counts >= 1.  A repeated id (two threads would update one logit), an id out
+    of order (the search for drafts would miss it) or a count of 0 is reported
+    per lane as SPEC_ERR_INVALID_ARG and that lane's logits stay as they were;
+    lanes with valid lists are penalised exactly as the oracle says, and a lane
+    whose offsets disagree with its draft length gets SPEC_ERR_LAYOUT."""
+    from gpu_harness import logits_to_numpy
+    from oracle import penalties as opn
+    rng = np.random.default_rng(17)
+    r = workloads.make_custom_round(617, DEV, lanes=6, vocab=5003, kmax=5, dtype="bf16", sampled="mixed",
+                                    fixed_k=True)
+    lists = []
+    for b in range(r.lanes):
+        ids = np.sort(rng.choice(r.vocab, size=40, replace=False)).astype(np.int32)
+        cnt = rng.integers(1, 4, size=40).astype(np.int32)
+        lists.append([ids, cnt])
+    lists[1][0][7] = lists[1][0][6]                      # a repeated id
+    lists[2][0][[3, 4]] = lists[2][0][[4, 3]]            # two ids out of order
+    lists[3][1][10] = 0                                  # a count of 0
+    toks = torch.tensor(np.concatenate([l[0] for l in lists]), dtype=torch.int32, device=DEV)
+    counts = torch.tensor(np.concatenate([l[1] for l in lists]), dtype=torch.int32, device=DEV)
+    offs = torch.tensor(np.arange(r.lanes + 1) * 40, dtype=torch.int64, device=DEV)
+    lens = r.draft_lens.clone()
+    lens[5] = 3                                          # offsets disagree with the draft length
+    pres = torch.full((r.lanes,), 0.75, dtype=torch.float32, device=DEV)
+    freq = torch.full((r.lanes,), 0.5, dtype=torch.float32, device=DEV)
+    status = torch.full((r.lanes,), -7, dtype=torch.int32, device=DEV)
+    before = logits_to_numpy(r.target, r.vocab)
+    sv.spec_apply_penalties(r.target, r.row_offsets, r.draft_tokens, lens, toks, counts, offs, pres, freq,
+                            lane_status=status)
+    torch.cuda.synchronize()
+    got = logits_to_numpy(r.target, r.vocab)
+    assert status.cpu().tolist() == [0, sv.SPEC_ERR_INVALID_ARG, sv.SPEC_ERR_INVALID_ARG, sv.SPEC_ERR_INVALID_ARG,
+                                     0, sv.SPEC_ERR_LAYOUT]
+    off = r.row_offsets.cpu().numpy()
+    want = opn.apply_penalties(before, "bf16", r.draft_tokens.cpu().numpy(), r.draft_lens.cpu().numpy(), off,
+                               toks.cpu().numpy(), counts.cpu().numpy(), offs.cpu().numpy(), pres.cpu().numpy(),
+                               freq.cpu().numpy())
+    for b in range(r.lanes):
+        rows = slice(off[b], off[b + 1])
+        if b in (0, 4):
+            np.testing.assert_array_equal(got[rows], want[rows])
+            assert (got[rows] != before[rows]).any()
+        else:
+            np.testing.assert_array_equal(got[rows], before[rows])
+
+
 def test_penalties_argument_errors():
     lib = sv.load_library()
-    assert lib.spec_apply_penalties(None, 1, 10, 10, -1, *([None] * 9)) == sv.SPEC_ERR_INVALID_ARG
-    assert lib.spec_apply_penalties(None, 1, 10, 10, 2, *([None] * 9)) == sv.SPEC_ERR_INVALID_ARG
-    assert lib.spec_apply_penalties(None, 1, 9, 10, 0, *([None] * 9)) == sv.SPEC_ERR_INVALID_ARG
-    assert lib.spec_apply_penalties(None, 7, 10, 10, 0, *([None] * 9)) == sv.SPEC_ERR_INVALID_ARG
-    assert lib.spec_apply_penalties(None, 1, 10, 10, 0, *([None] * 9)) == sv.SPEC_OK
+    assert lib.spec_apply_penalties(None, 1, 10, 10, -1, *([None] * 10)) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_apply_penalties(None, 1, 10, 10, 2, *([None] * 10)) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_apply_penalties(None, 1, 9, 10, 0, *([None] * 10)) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_apply_penalties(None, 7, 10, 10, 0, *([None] * 10)) == sv.SPEC_ERR_INVALID_ARG
+    assert lib.spec_apply_penalties(None, 1, 10, 10, 0, *([None] * 10)) == sv.SPEC_OK
 
 
 def test_mean_committed_count_follows_the_closed_form():
