@@ -85,9 +85,8 @@ constexpr uint32_t kBadValue = 1u;  // NaN or +inf in the row
 constexpr uint32_t kTimedOut = 2u;  // a bounded wait gave up
 
 struct __align__(16) DrawPartial {
-  float w;     // sum of draw weights over one CTA's slice
-  int last;    // largest index of positive weight in the slice (-1 if none)
-  int pad0, pad1;
+  float w;  // sum of draw weights over one CTA's slice
+  int pad0, pad1, pad2;
 };
 
 enum DrawMode : int { kNoDraw = 0, kResidual = 1, kBonus = 2 };
@@ -103,7 +102,6 @@ struct __align__(16) SmemHead {
   Partial fin[kMaxStreams];                    // this CTA's partial, then the lane's total
   DrawPartial dpart[2][kMaxCluster];           // pass-2 slice sums (pushed by peers)
   float segsum[kConsumerWarps];
-  int seglast[kConsumerWarps];
   int drafts[kMaxDrafts + 1];
   float xd_t[kMaxDrafts + 1];  // target logit at d_{j+1} in row j
   float xd_q[kMaxDrafts + 1];  // drafter logit at d_{j+1} in row j
@@ -590,24 +588,60 @@ __device__ __forceinline__ CompSum log2_prob_terms(float xd, const Partial& row,
 // ---------------------------------------------------------------------------
 // Pass-2 draw weights
 // ---------------------------------------------------------------------------
+// The weight of element x is p(x) for a bonus draw and max(0, p(x) - q(x)) for
+// a residual draw, with p(x) = 2^(fl(fl(x * c - fl(m_p * c)) - log2 S_p)) and
+// q the same over the drafter row.  The sums take the weights as packed pairs
+// and the walk as scalars; both round every step identically, so each weight
+// has the same bits wherever it is formed, and a lane's eight weights are
+// always added in the same order (tree8).
 struct DrawCoef {
   float mp, l2sp;  // target row: scaled reference fl(max * c) and log2 of its sum
   float mq, l2sq;  // drafter row (residual only)
   float c;         // log2(e) / T
-  bool residual;
 };
 
-// Normalised probability 2^(x * c - fl(m * c) - log2 S), evaluated with
-// explicit roundings so that both call sites produce identical bits.
-__device__ __forceinline__ float prob_at(float x, float mr, float l2s, float c) {
-  return ex2_approx(__fsub_rn(__fmaf_rn(x, c, -mr), l2s));
+template <bool RESID>
+__device__ __forceinline__ float draw_weight(const DrawCoef& k, float xt, float xq) {
+  const float p = ex2_approx(__fsub_rn(__fmaf_rn(xt, k.c, -k.mp), k.l2sp));
+  if (!RESID) return p;
+  const float q = ex2_approx(__fsub_rn(__fmaf_rn(xq, k.c, -k.mq), k.l2sq));
+  return fmaxf(0.f, __fsub_rn(p, q));
 }
 
-__device__ __forceinline__ float draw_weight(const DrawCoef& k, float xt, float xq) {
-  const float p = prob_at(xt, k.mp, k.l2sp, k.c);
-  if (!k.residual) return p;
-  const float q = prob_at(xq, k.mq, k.l2sq, k.c);
-  return fmaxf(0.f, __fsub_rn(p, q));
+// The coefficients duplicated into packed pairs.
+struct DrawCoef2 {
+  unsigned long long c, nmp, nl2sp, nmq, nl2sq, neg1;
+};
+
+__device__ __forceinline__ DrawCoef2 pack_coef(const DrawCoef& k) {
+  DrawCoef2 r;
+  r.c = f2_pack(k.c, k.c);
+  r.nmp = f2_pack(-k.mp, -k.mp);
+  r.nl2sp = f2_pack(-k.l2sp, -k.l2sp);
+  r.nmq = f2_pack(-k.mq, -k.mq);
+  r.nl2sq = f2_pack(-k.l2sq, -k.l2sq);
+  r.neg1 = f2_pack(-1.f, -1.f);
+  return r;
+}
+
+// draw_weight of two elements at once: x - l2s is added as x + (-l2s), and
+// p - q formed as fma(q, -1, p), both rounded once, as the scalar forms are.
+template <bool RESID>
+__device__ __forceinline__ unsigned long long draw_weight2(const DrawCoef2& k, unsigned long long xt,
+                                                           unsigned long long xq) {
+  const unsigned long long p = f2_ex2(f2_add(f2_fma(xt, k.c, k.nmp), k.nl2sp));
+  if (!RESID) return p;
+  const unsigned long long q = f2_ex2(f2_add(f2_fma(xq, k.c, k.nmq), k.nl2sq));
+  float lo, hi;
+  f2_unpack(f2_fma(q, k.neg1, p), lo, hi);
+  return f2_pack(fmaxf(0.f, lo), fmaxf(0.f, hi));
+}
+
+// Total of a lane's eight weights: ((w0 + w2) + (w4 + w6)) + ((w1 + w3) + (w5 + w7)),
+// the order in which the packed pairs add them.
+__device__ __forceinline__ float tree8(const float (&w)[8]) {
+  return __fadd_rn(__fadd_rn(__fadd_rn(w[0], w[2]), __fadd_rn(w[4], w[6])),
+                   __fadd_rn(__fadd_rn(w[1], w[3]), __fadd_rn(w[5], w[7])));
 }
 
 // Eight consecutive logits of a row, kept as raw bits (one 16-byte vector of
@@ -621,6 +655,18 @@ template <typename T>
 __device__ __forceinline__ float raw_elem(const Raw8<T>& r, int i) {
   if constexpr (ElemTraits<T>::kVec == 8) return vec_elem<T>(r.v[0], i);
   else return vec_elem<T>(r.v[i >> 2], i & 3);
+}
+
+// Elements 2j and 2j + 1 as a packed pair.
+template <typename T>
+__device__ __forceinline__ unsigned long long raw_pair(const Raw8<T>& r, int j) {
+  if constexpr (ElemTraits<T>::kVec == 8) {
+    return bf16_pair((j == 0) ? r.v[0].x : (j == 1) ? r.v[0].y : (j == 2) ? r.v[0].z : r.v[0].w);
+  } else {
+    const uint4 v = r.v[j >> 1];
+    return (j & 1) ? f2_pack(__uint_as_float(v.z), __uint_as_float(v.w))
+                   : f2_pack(__uint_as_float(v.x), __uint_as_float(v.y));
+  }
 }
 
 // Elements e .. e+7 of a row; those at or past `end` read as -inf.
@@ -652,25 +698,39 @@ __device__ __forceinline__ void load_raw8(const uint8_t* row, int e, int end, Ra
   }
 }
 
-// The eight draw weights of one lane's piece of a pass-2 round, and their
-// running sums in element order (cum[7] is the piece's total).
-template <typename T>
-__device__ __forceinline__ void draw_piece(const DrawCoef& k, const Raw8<T>& rt, const Raw8<T>& rq, int e,
-                                           int end, float (&w)[8], float (&cum)[8]) {
-  float run = 0.f;
+// Total of the weights of one lane's eight elements, all in range, as packed pairs.
+template <typename T, bool RESID>
+__device__ __forceinline__ float piece_total(const DrawCoef2& k, const Raw8<T>& rt, const Raw8<T>& rq) {
+  unsigned long long w2[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if constexpr (RESID) w2[j] = draw_weight2<true>(k, raw_pair<T>(rt, j), raw_pair<T>(rq, j));
+    else w2[j] = draw_weight2<false>(k, raw_pair<T>(rt, j), 0ull);
+  }
+  float lo, hi;
+  f2_unpack(f2_add(f2_add(w2[0], w2[1]), f2_add(w2[2], w2[3])), lo, hi);
+  return __fadd_rn(lo, hi);
+}
+
+// The eight weights of elements e .. e+7 (0 at or past `end`) as scalars.
+template <typename T, bool RESID>
+__device__ __forceinline__ void piece_weights(const DrawCoef& k, const Raw8<T>& rt, const Raw8<T>& rq, int e, int end,
+                                              float (&w)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    w[i] = (e + i < end) ? draw_weight(k, raw_elem<T>(rt, i), k.residual ? raw_elem<T>(rq, i) : -INFINITY) : 0.f;
-    run = __fadd_rn(run, w[i]);
-    cum[i] = run;
+    if constexpr (RESID) w[i] = (e + i < end) ? draw_weight<true>(k, raw_elem<T>(rt, i), raw_elem<T>(rq, i)) : 0.f;
+    else w[i] = (e + i < end) ? draw_weight<false>(k, raw_elem<T>(rt, i), 0.f) : 0.f;
   }
 }
 
-// Pass-2 rounds whose loads are issued together (fp32 rounds hold twice the
-// registers).
+// Pass-2 rounds whose loads are issued together: one round's loads are in
+// flight while the previous round is summed.  (Four rounds, two in flight,
+// pushed the 20-warp builds past their 80 registers into spills, which cost
+// more than the extra latency hidden: the ragged 128-lane round 92.7 against
+// 84.7 us.)
 template <typename T>
 __host__ __device__ constexpr int draw_batch() {
-  return ElemTraits<T>::kVec == 8 ? 4 : 2;
+  return 2;
 }
 
 __device__ __forceinline__ float warp_sum_xor(float v) {
@@ -683,6 +743,146 @@ __device__ __forceinline__ int warp_max_int(int v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
+}
+
+// One warp's pass-2 segment [s0, s1) is taken in rounds of kDrawRound
+// elements; lane l holds elements 8l .. 8l+7 of each round.  `lsum`, when
+// given, keeps every lane's total of every round (lsum[r * 32 + lane]).
+
+// Sum of the draw weights of the segment (every lane gets it).  Full rounds
+// run as packed pairs with the next half-batch's loads in flight; the last,
+// partial round is masked.
+template <typename T, bool ALIGNED, bool RESID>
+__device__ __forceinline__ float draw_segment_sum(const DrawCoef& kc, const uint8_t* trow, const uint8_t* qrow,
+                                                  int s0, int s1, float* lsum, int lane) {
+  constexpr int kHalf = draw_batch<T>() / 2;
+  const DrawCoef2 k2 = pack_coef(kc);
+  const int nfull = (s1 > s0) ? (s1 - s0) / kDrawRound : 0;
+  float acc = 0.f;
+  Raw8<T> rtA[kHalf], rqA[kHalf], rtB[kHalf], rqB[kHalf];
+  auto load_half = [&](Raw8<T> (&rt)[kHalf], Raw8<T> (&rq)[kHalf], int r0) {
+#pragma unroll
+    for (int u = 0; u < kHalf; ++u) {
+      if (r0 + u < nfull) {
+        const int e = s0 + (r0 + u) * kDrawRound + lane * 8;
+        load_raw8<T, ALIGNED>(trow, e, s1, rt[u]);
+        if constexpr (RESID) load_raw8<T, ALIGNED>(qrow, e, s1, rq[u]);
+      }
+    }
+  };
+  auto sum_half = [&](const Raw8<T> (&rt)[kHalf], const Raw8<T> (&rq)[kHalf], int r0) {
+#pragma unroll
+    for (int u = 0; u < kHalf; ++u) {
+      if (r0 + u < nfull) {
+        const float t = piece_total<T, RESID>(k2, rt[u], rq[u]);
+        if (lsum) lsum[(r0 + u) * 32 + lane] = t;
+        acc = __fadd_rn(acc, t);
+      }
+    }
+  };
+  if (nfull > 0) load_half(rtA, rqA, 0);
+  for (int r = 0; r < nfull; r += 2 * kHalf) {
+    if (r + kHalf < nfull) load_half(rtB, rqB, r + kHalf);
+    sum_half(rtA, rqA, r);
+    if (r + kHalf >= nfull) break;
+    if (r + 2 * kHalf < nfull) load_half(rtA, rqA, r + 2 * kHalf);
+    sum_half(rtB, rqB, r + kHalf);
+  }
+  const int tb = s0 + nfull * kDrawRound;
+  if (tb < s1) {
+    const int e = tb + lane * 8;
+    Raw8<T> rt, rq;
+    load_raw8<T, ALIGNED>(trow, e, s1, rt);
+    if constexpr (RESID) load_raw8<T, ALIGNED>(qrow, e, s1, rq);
+    float w[8];
+    piece_weights<T, RESID>(kc, rt, rq, e, s1, w);
+    const float t = tree8(w);
+    if (lsum) lsum[nfull * 32 + lane] = t;
+    acc = __fadd_rn(acc, t);
+  }
+  return warp_sum_xor(acc);
+}
+
+// This lane's eight weights of the round at `base`, and their total (equal,
+// bit for bit, to what draw_segment_sum took for it).
+template <typename T, bool ALIGNED, bool RESID>
+__device__ __forceinline__ float draw_round_weights(const DrawCoef& kc, const uint8_t* trow, const uint8_t* qrow,
+                                                    int base, int s1, int lane, float (&w)[8]) {
+  const int e = base + lane * 8;
+  Raw8<T> rt, rq;
+  load_raw8<T, ALIGNED>(trow, e, s1, rt);
+  if constexpr (RESID) load_raw8<T, ALIGNED>(qrow, e, s1, rq);
+  piece_weights<T, RESID>(kc, rt, rq, e, s1, w);
+  return tree8(w);
+}
+
+// Largest index of positive weight in the segment (-1 if none): the last
+// round, then the last lane, holding weight.  Whole warp.
+template <typename T, bool ALIGNED, bool RESID>
+__device__ __noinline__ int draw_last_positive(const DrawCoef& kc, const uint8_t* trow, const uint8_t* qrow, int s0,
+                                               int s1, const float* lsum, int lane) {
+  const int nr = (s1 > s0) ? (s1 - s0 + kDrawRound - 1) / kDrawRound : 0;
+  float w[8];
+  for (int r = nr - 1; r >= 0; --r) {
+    const int base = s0 + r * kDrawRound;
+    const float lt = lsum ? lsum[r * 32 + lane] : draw_round_weights<T, ALIGNED, RESID>(kc, trow, qrow, base, s1, lane, w);
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, lt > 0.f);
+    if (m) {
+      if (lsum) draw_round_weights<T, ALIGNED, RESID>(kc, trow, qrow, base, s1, lane, w);
+      const int l = 31 - __clz(m);
+      int pos = -1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (w[i] > 0.f) pos = base + lane * 8 + i;
+      return __shfl_sync(0xFFFFFFFFu, pos, l);
+    }
+  }
+  return -1;
+}
+
+// Index of the element at which the running weight sum of the segment first
+// exceeds tau: the round from the round totals, the lane from a scan of the
+// lane totals, the element from the lane's own running sum; -2 if no round
+// crosses.  Where rounding leaves a round (or a lane) with no crossing
+// element, the last element of positive weight in it.  Whole warp.
+template <typename T, bool ALIGNED, bool RESID>
+__device__ __noinline__ int draw_walk(const DrawCoef& kc, const uint8_t* trow, const uint8_t* qrow, int s0, int s1,
+                                      const float* lsum, float tau, int lane) {
+  const int nr = (s1 > s0) ? (s1 - s0 + kDrawRound - 1) / kDrawRound : 0;
+  float run = 0.f;
+  float w[8];
+  for (int r = 0; r < nr; ++r) {
+    const int base = s0 + r * kDrawRound;
+    const float lt = lsum ? lsum[r * 32 + lane] : draw_round_weights<T, ALIGNED, RESID>(kc, trow, qrow, base, s1, lane, w);
+    const float next = __fadd_rn(run, warp_sum_xor(lt));
+    if (next > tau) {
+      if (lsum) draw_round_weights<T, ALIGNED, RESID>(kc, trow, qrow, base, s1, lane, w);
+      const float tau2 = __fsub_rn(tau, run);
+      float incl = lt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float up = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl = __fadd_rn(up, incl);
+      }
+      float excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+      if (lane == 0) excl = 0.f;
+      const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl > tau2);
+      const uint32_t pos_lanes = __ballot_sync(0xFFFFFFFFu, lt > 0.f);
+      const int l = hit ? (__ffs(hit) - 1) : (pos_lanes ? 31 - __clz(pos_lanes) : 0);
+      const float tau3 = __fsub_rn(tau2, excl);
+      int t = -1, lastpos = -1;
+      float cum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cum = __fadd_rn(cum, w[i]);
+        if (w[i] > 0.f) lastpos = base + lane * 8 + i;
+        if (hit && t < 0 && cum > tau3) t = base + lane * 8 + i;
+      }
+      return __shfl_sync(0xFFFFFFFFu, (t >= 0) ? t : lastpos, l);
+    }
+    run = next;
+  }
+  return -2;
 }
 
 // ---------------------------------------------------------------------------
@@ -1305,34 +1505,35 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   if (sh.scan_mode == kNoDraw) return;
 
   // ---- pass 2: draw the model's token (sampled lanes, whole cluster) ----
-  constexpr int kDrawBatch = draw_batch<T>();
   const int n = sh.scan_n;
   bool residual = (sh.scan_mode == kResidual);
   int draw_row = residual ? n : k;  // target row whose p enters the weights
   const uint8_t* qrow = p.draft + static_cast<int64_t>(off + n) * p.ld_bytes;
   const float uprime = sh.u_smp[n];
-  // Each consumer warp walks one segment of the slice (a multiple of 8
+  // Each consumer warp takes one segment of the slice (a multiple of 8
   // elements, so rounds start 16-byte aligned; the last round may be partial).
 #ifndef SPEC_VERIFY_SEG_ROUND
 #define SPEC_VERIFY_SEG_ROUND 256
 #endif
   const int seg = ((span + kConsumerWarps - 1) / kConsumerWarps + SPEC_VERIFY_SEG_ROUND - 1) /
                   SPEC_VERIFY_SEG_ROUND * SPEC_VERIFY_SEG_ROUND;
-  // Each warp keeps the weight sum of every round of its segment in the ring
-  // (free after pass 1), so that the warp holding the crossing later re-reads
-  // one round instead of walking its segment.  Unaligned launches have no
-  // ring; they, and segments with more rounds than fit, walk the segment.
+  // Every lane's total of every round of its warp's segment is kept in the
+  // ring (free after pass 1), so that the walk re-reads one lane's eight
+  // elements only.  Unaligned launches have no ring; they, and segments with
+  // more rounds than fit, recompute the round totals they walk over.
   const int seg_rounds = (seg + kDrawRound - 1) / kDrawRound;
-  float* round_sums = reinterpret_cast<float*>(ring);
-  const bool keep_rounds = ALIGNED && static_cast<int64_t>(seg_rounds) * kConsumerWarps * 4 <=
+  float* lane_sums = reinterpret_cast<float*>(ring);
+  const bool keep_rounds = ALIGNED && static_cast<int64_t>(seg_rounds) * kConsumerWarps * 32 * 4 <=
                                           static_cast<int64_t>(nslots) * p.slot_bytes;
+  auto seg_lsum = [&](int w) -> float* {
+    return keep_rounds ? lane_sums + static_cast<int64_t>(w) * seg_rounds * 32 : nullptr;
+  };
   auto make_coef = [&]() {
     DrawCoef kc;
     const Partial pt = sh.fin[2 * draw_row];
     kc.mp = scaled_ref(pt.m, c);
     kc.l2sp = log2f(pt.s);
     kc.c = c;
-    kc.residual = residual;
     kc.mq = 0.f;
     kc.l2sq = 0.f;
     if (residual) {
@@ -1353,73 +1554,20 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     if (warp < kConsumerWarps) {
       const int s0 = v0 + warp * seg;
       const int s1 = min(v1, s0 + seg);
-      float segw = 0.f;
-      int last = -1;
-      // Software-pipelined in two halves of kDrawBatch rounds: the loads of
-      // the next half are in flight while this half is computed.
-      constexpr int kHalf = kDrawBatch / 2;
-      Raw8<T> rtA[kHalf], rqA[kHalf], rtB[kHalf], rqB[kHalf];
-      auto load_half = [&](Raw8<T> (&rt)[kHalf], Raw8<T> (&rq)[kHalf], int base) {
-#pragma unroll
-        for (int u = 0; u < kHalf; ++u) {
-          const int e = base + u * kDrawRound + lane * 8;
-          if (base + u * kDrawRound < s1) {
-            load_raw8<T, ALIGNED>(trow, e, s1, rt[u]);
-            if (kc.residual) load_raw8<T, ALIGNED>(qrow, e, s1, rq[u]);
-          }
-        }
-      };
-      auto sum_half = [&](const Raw8<T> (&rt)[kHalf], const Raw8<T> (&rq)[kHalf], int base) {
-#pragma unroll
-        for (int u = 0; u < kHalf; ++u) {
-          if (base + u * kDrawRound >= s1) break;
-          float w[8], cum[8];
-          const int e = base + u * kDrawRound + lane * 8;
-          draw_piece<T>(kc, rt[u], rq[u], e, s1, w, cum);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (w[i] > 0.f) last = e + i;
-          const float R = warp_sum_xor(cum[7]);
-          if (keep_rounds && lane == 0) round_sums[warp * seg_rounds + (base - s0) / kDrawRound + u] = R;
-          segw = __fadd_rn(segw, R);
-        }
-      };
-      constexpr int kStep = kHalf * kDrawRound;
-      if (seg_rounds <= kDrawBatch) {
-        // A segment of one batch: every load first, then the sums.
-        if (s0 < s1) load_half(rtA, rqA, s0);
-        if (s0 + kStep < s1) load_half(rtB, rqB, s0 + kStep);
-        if (s0 < s1) sum_half(rtA, rqA, s0);
-        if (s0 + kStep < s1) sum_half(rtB, rqB, s0 + kStep);
-      } else {
-        if (s0 < s1) load_half(rtA, rqA, s0);
-        for (int base = s0; base < s1; base += 2 * kStep) {
-          if (base + kStep < s1) load_half(rtB, rqB, base + kStep);
-          sum_half(rtA, rqA, base);
-          if (base + kStep >= s1) break;
-          if (base + 2 * kStep < s1) load_half(rtA, rqA, base + 2 * kStep);
-          sum_half(rtB, rqB, base + kStep);
-        }
-      }
-      last = warp_max_int(last);
-      if (lane == 0) {
-        sh.segsum[warp] = segw;
-        sh.seglast[warp] = last;
-      }
+      const float segw = residual
+                             ? draw_segment_sum<T, ALIGNED, true>(kc, trow, qrow, s0, s1, seg_lsum(warp), lane)
+                             : draw_segment_sum<T, ALIGNED, false>(kc, trow, qrow, s0, s1, seg_lsum(warp), lane);
+      if (lane == 0) sh.segsum[warp] = segw;
     }
     __syncthreads();
     if (tid < C) {
       float wc = 0.f;
-      int lc = -1;
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        wc = __fadd_rn(wc, sh.segsum[w]);
-        lc = max(lc, sh.seglast[w]);
-      }
+      for (int w = 0; w < kConsumerWarps; ++w) wc = __fadd_rn(wc, sh.segsum[w]);
       if (tid == static_cast<int>(rank)) {
-        sh.dpart[buf][rank] = DrawPartial{wc, lc, 0, 0};
+        sh.dpart[buf][rank] = DrawPartial{wc, 0, 0, 0};
       } else {
-        st_async_v4(cluster_map(&sh.dpart[buf][rank], tid), __float_as_uint(wc), static_cast<uint32_t>(lc),
-                    0u, 0u, cluster_map(&sh.dbar[buf], tid));
+        st_async_v4(cluster_map(&sh.dpart[buf][rank], tid), __float_as_uint(wc), 0u, 0u, 0u,
+                    cluster_map(&sh.dbar[buf], tid));
       }
     }
     if (tid == 0 && !mbar_wait_bounded(&sh.dbar[buf], 0, kExchangeWaitLimitNs)) {
@@ -1443,7 +1591,10 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     __syncthreads();
   }
 
-  // CTA holding the crossing of u' * W (cumulative sums in CTA order).
+  // The CTA holding the crossing of u' * W (cumulative sums in CTA order),
+  // and in it the warp whose segment holds it; where rounding leaves no
+  // crossing, the last element of positive weight (in the last CTA, and
+  // then the last warp, holding weight).
   const float target = __fmul_rn(uprime, W);
   int owner = -1;
   float prefix = 0.f;
@@ -1455,132 +1606,52 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     }
     prefix = next;
   }
-  int token = -1;
-  bool write = false;
+  auto last_warp_with_weight = [&]() {
+    int lw = -1;
+    for (int w = 0; w < kConsumerWarps; ++w)
+      if (sh.segsum[w] > 0.f) lw = w;
+    return lw;
+  };
+  int fw = -1;         // the warp that finds the token in this CTA
+  float tau_w = -1.f;  // its threshold within its segment (< 0: the last positive weight)
   if (owner < 0) {
-    // Rounding left no crossing: the largest index of positive weight.
     int last_r = -1;
     for (int r = 0; r < C; ++r)
       if (sh.dpart[buf][r].w > 0.f) last_r = r;
-    if (last_r == static_cast<int>(rank) && tid == 0) {
-      token = sh.dpart[buf][rank].last;
-      write = true;
-    }
+    if (last_r == static_cast<int>(rank)) fw = last_warp_with_weight();
   } else if (owner == static_cast<int>(rank)) {
     const float tau = __fsub_rn(target, prefix);
-    int wsel = -1;
     float q = 0.f;
     for (int w = 0; w < kConsumerWarps; ++w) {
       const float next = __fadd_rn(q, sh.segsum[w]);
       if (next > tau) {
-        wsel = w;
+        fw = w;
+        tau_w = __fsub_rn(tau, q);
         break;
       }
       q = next;
     }
-    if (wsel < 0) {
-      if (tid == 0) {
-        int lc = -1;
-        for (int w = 0; w < kConsumerWarps; ++w) lc = max(lc, sh.seglast[w]);
-        token = lc;
-        write = true;
-      }
-    } else if (warp == wsel) {
-      const DrawCoef kc = make_coef();
-      const uint8_t* trow = p.target + static_cast<int64_t>(off + draw_row) * p.ld_bytes;
-      const float tau1 = __fsub_rn(tau, q);
-      int s0 = v0 + warp * seg;
-      int s1 = min(v1, s0 + seg);
-      float run = 0.f;
-      int found = -1;
-      if (keep_rounds) {
-        // The round whose sum takes the running total past tau1, from the
-        // sums the same warp took in the same order; only it is re-read.
-        const int nr = (s1 - s0 + kDrawRound - 1) / kDrawRound;
-        int r = 0;
-        for (; r < nr; ++r) {
-          const float R = round_sums[warp * seg_rounds + r];
-          const float next = __fadd_rn(run, R);
-          if (next > tau1) break;
-          run = next;
-        }
-        if (r == nr) {
-          s0 = s1;  // no crossing: the segment's last positive weight below
-        } else {
-          s0 += r * kDrawRound;
-          s1 = min(s1, s0 + kDrawRound);
-        }
-      }
-      for (int bbase = s0; bbase < s1 && found < 0; bbase += kDrawBatch * kDrawRound) {
-        Raw8<T> rt[kDrawBatch], rq[kDrawBatch];
-#pragma unroll
-        for (int u = 0; u < kDrawBatch; ++u) {
-          const int e = bbase + u * kDrawRound + lane * 8;
-          if (bbase + u * kDrawRound < s1) {
-            load_raw8<T, ALIGNED>(trow, e, s1, rt[u]);
-            if (kc.residual) load_raw8<T, ALIGNED>(qrow, e, s1, rq[u]);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kDrawBatch; ++u) {
-          const int base = bbase + u * kDrawRound;
-          if (base >= s1 || found >= 0) break;
-          float w[8], cum[8];
-          const int e = base + lane * 8;
-          draw_piece<T>(kc, rt[u], rq[u], e, s1, w, cum);
-          const float R = warp_sum_xor(cum[7]);
-          const float next = __fadd_rn(run, R);
-          if (next > tau1) {
-            // The crossing is in this round: inclusive scan over the lanes.
-            const float tau2 = __fsub_rn(tau1, run);
-            float incl = cum[7];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const float up = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-              if (lane >= o) incl = __fadd_rn(up, incl);
-            }
-            float excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-            if (lane == 0) excl = 0.f;
-            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl > tau2);
-            int tok = -1;
-            if (hit) {
-              const int l = __ffs(hit) - 1;
-              if (lane == l) {
-                const float tau3 = __fsub_rn(tau2, excl);
-                int t = -1, lastpos = -1;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  if (w[i] > 0.f) lastpos = e + i;
-                  if (t < 0 && cum[i] > tau3) t = e + i;
-                }
-                tok = (t >= 0) ? t : lastpos;
-              }
-              tok = __shfl_sync(0xFFFFFFFFu, tok, l);
-            } else {
-              int lastpos = -1;
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                if (w[i] > 0.f) lastpos = e + i;
-              tok = warp_max_int(lastpos);
-            }
-            found = tok;
-          }
-          run = next;
-        }
-      }
-      if (found < 0) found = sh.seglast[warp];
-      if (lane == 0) {
-        token = found;
-        write = true;
-      }
-    }
+    if (fw < 0) fw = last_warp_with_weight();
   }
-  if (write) {
-    p.out_tokens[off + n] = token;
-    if (p.row_stats) {
-      spec_row_stats* rs = p.row_stats + off + n;
-      rs->drawn = token;
-      if (sh.scan_mode == kResidual) rs->resid_mass = resid_mass;
+  if (fw >= 0 && warp == fw) {
+    const DrawCoef kc = make_coef();
+    const uint8_t* trow = p.target + static_cast<int64_t>(off + draw_row) * p.ld_bytes;
+    const int s0 = v0 + warp * seg;
+    const int s1 = min(v1, s0 + seg);
+    int token = -2;
+    if (tau_w >= 0.f)
+      token = residual ? draw_walk<T, ALIGNED, true>(kc, trow, qrow, s0, s1, seg_lsum(warp), tau_w, lane)
+                       : draw_walk<T, ALIGNED, false>(kc, trow, qrow, s0, s1, seg_lsum(warp), tau_w, lane);
+    if (token == -2)
+      token = residual ? draw_last_positive<T, ALIGNED, true>(kc, trow, qrow, s0, s1, seg_lsum(warp), lane)
+                       : draw_last_positive<T, ALIGNED, false>(kc, trow, qrow, s0, s1, seg_lsum(warp), lane);
+    if (lane == 0) {
+      p.out_tokens[off + n] = token;
+      if (p.row_stats) {
+        spec_row_stats* rs = p.row_stats + off + n;
+        rs->drawn = token;
+        if (sh.scan_mode == kResidual) rs->resid_mass = resid_mass;
+      }
     }
   }
 }
