@@ -158,6 +158,27 @@ const KernelVariant& variant(int which) {
 
 int kernel_index(int dtype, bool aligned) { return dtype * 2 + (aligned ? 1 : 0); }
 
+// Rounds without drafter logits whose rows are at most this many bytes run on
+// the small-round kernel (one CTA per lane, plain loads): the 1-lane round of
+// four 4 KB rows takes 2.45 us on the cluster kernel, which sets up a cluster,
+// a ring and its barriers for 16 KB.  A forced build or cluster size, or
+// SPEC_VERIFY_SMALL=0, keeps the cluster kernel.
+constexpr int kSmallRowBytes = 16 * 1024;
+
+bool use_small(bool with_draft, int V, int esize) {
+  if (with_draft || static_cast<int64_t>(V) * esize > kSmallRowBytes) return false;
+  if (env_int("SPEC_VERIFY_SMALL", 1) == 0) return false;
+  return forced_build() < 0 && env_int("SPEC_VERIFY_CLUSTER", 0) <= 0;
+}
+
+void* small_kernel(int dtype, bool aligned) {
+  static void* const k[4] = {reinterpret_cast<void*>(&specv::verify_small_kernel<float, false>),
+                             reinterpret_cast<void*>(&specv::verify_small_kernel<float, true>),
+                             reinterpret_cast<void*>(&specv::verify_small_kernel<bf16_tag, false>),
+                             reinterpret_cast<void*>(&specv::verify_small_kernel<bf16_tag, true>)};
+  return k[kernel_index(dtype, aligned)];
+}
+
 bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Clusters that can be resident at once, per device / kernel / cluster size /
@@ -285,6 +306,47 @@ int resolve_launch(DeviceCache* dc, int dev, bool with_draft, int lanes, int row
   return rc;
 }
 
+// The small-round launch: one CTA per lane, programmatic dependent launch as
+// for the cluster kernel.
+int launch_small(const spec_verify_args* a, int esize, bool aligned, void* stream) {
+  specv::VerifyParams p{};
+  p.target = static_cast<const uint8_t*>(a->target_logits);
+  p.draft = nullptr;
+  p.ld_bytes = a->ld * esize;
+  p.V = a->V;
+  p.lanes = a->lanes;
+  p.rows = a->rows;
+  p.draft_tokens = a->draft_tokens;
+  p.draft_lens = a->draft_lens;
+  p.row_offsets = a->row_offsets;
+  p.temps = a->temperatures;
+  p.seed = a->seed;
+  p.committed = a->committed;
+  p.out_tokens = a->out_tokens;
+  p.lane_status = a->lane_status;
+  p.row_stats = a->row_stats;
+  p.lane_base = a->lane_base;
+  p.flags = a->flags;
+  p.cluster = 1;
+  p.slice = a->V;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a->lanes), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(specv::kSmallThreads), 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  void* kargs[] = {&p};
+  if (cudaLaunchKernelExC(&cfg, small_kernel(a->dtype, aligned), kargs) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -333,6 +395,13 @@ int spec_verify_launch_shape(int32_t lanes, int32_t rows, int32_t V, spec_dtype 
   DeviceCache* dc = nullptr;
   int dev = 0;
   if (device_cache(&dc, &dev) != SPEC_OK) return SPEC_ERR_CUDA;
+  if (use_small(with_draft != 0, V, dtype == SPEC_BF16 ? 2 : 4)) {
+    if (cluster_ctas) *cluster_ctas = 1;
+    if (threads) *threads = specv::kSmallThreads;
+    if (slice) *slice = V;
+    if (smem_bytes) *smem_bytes = 0;
+    return SPEC_OK;
+  }
   VerifyShape s{};
   int which = 0;
   const int rc = resolve_launch(dc, dev, with_draft != 0, lanes, rows, V, dtype, true, &s, nullptr, &which);
@@ -362,6 +431,7 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
   const bool aligned = is_aligned16(a->target_logits) &&
                        (a->draft_logits == nullptr || is_aligned16(a->draft_logits)) &&
                        ((a->ld * esize) % 16 == 0);
+  if (use_small(a->draft_logits != nullptr, a->V, esize)) return launch_small(a, esize, aligned, stream);
   VerifyShape s{};
   void* kernel = nullptr;
   int which = 0;

@@ -102,6 +102,7 @@ struct __align__(16) SmemHead {
   Partial fin[kMaxStreams];                    // this CTA's partial, then the lane's total
   DrawPartial dpart[2][kMaxCluster];           // pass-2 slice sums (pushed by peers)
   float segsum[kConsumerWarps];
+  float dcoef[5];  // pass-2 weight coefficients (DrawCoef) of the current attempt
   int drafts[kMaxDrafts + 1];
   float xd_t[kMaxDrafts + 1];  // target logit at d_{j+1} in row j
   float xd_q[kMaxDrafts + 1];  // drafter logit at d_{j+1} in row j
@@ -600,6 +601,32 @@ struct DrawCoef {
   float c;         // log2(e) / T
 };
 
+// Coefficients of the weights of a draw from target row `rt` (and drafter row
+// `rq` for a residual draw, -1 for a bonus draw) given the rows' totals.
+__device__ __forceinline__ void draw_coef_store(float* out, const Partial* fin, int rt, int rq, float c) {
+  const Partial pt = fin[2 * rt];
+  out[0] = scaled_ref(pt.m, c);
+  out[1] = log2f(pt.s);
+  out[2] = 0.f;
+  out[3] = 0.f;
+  out[4] = c;
+  if (rq >= 0) {
+    const Partial pq = fin[2 * rq + 1];
+    out[2] = scaled_ref(pq.m, c);
+    out[3] = log2f(pq.s);
+  }
+}
+
+__device__ __forceinline__ DrawCoef draw_coef_load(const float* in) {
+  DrawCoef k;
+  k.mp = in[0];
+  k.l2sp = in[1];
+  k.mq = in[2];
+  k.l2sq = in[3];
+  k.c = in[4];
+  return k;
+}
+
 template <bool RESID>
 __device__ __forceinline__ float draw_weight(const DrawCoef& k, float xt, float xq) {
   const float p = ex2_approx(__fsub_rn(__fmaf_rn(xt, k.c, -k.mp), k.l2sp));
@@ -912,13 +939,13 @@ __device__ __forceinline__ void push_partials(SmemHead& sh, int nstreams, int C,
 // the lane's combined keys: lane j has the key of row j and `flags` is the
 // OR of every CTA's flags.  Draft d_{j+1} is accepted while it equals the
 // argmax of row j; the committed tokens are the argmaxes of rows 0..n.
-__device__ __forceinline__ void greedy_finish(const VerifyParams& p, const SmemHead& sh, int b, int k, int off,
+__device__ __forceinline__ void greedy_finish(const VerifyParams& p, const int* drafts, int b, int k, int off,
                                               int status, unsigned long long key, uint32_t flags, int lane) {
   float m;
   int a;
   argmax_key_decode(key, m, a);
   int st = status;
-  const bool range_bad = (st == SPEC_OK) && lane < k && (sh.drafts[lane] < 0 || sh.drafts[lane] >= p.V);
+  const bool range_bad = (st == SPEC_OK) && lane < k && (drafts[lane] < 0 || drafts[lane] >= p.V);
   const bool empty_row = (st == SPEC_OK) && lane <= k && key == 0ull;
   const bool any_range_bad = __any_sync(0xFFFFFFFFu, range_bad);
   const bool any_empty = __any_sync(0xFFFFFFFFu, empty_row);
@@ -927,7 +954,7 @@ __device__ __forceinline__ void greedy_finish(const VerifyParams& p, const SmemH
     else if (flags & kTimedOut) st = SPEC_ERR_TIMEOUT;
     else if ((flags & kBadValue) || any_empty) st = SPEC_ERR_NONFINITE;
   }
-  const bool stop = (st == SPEC_OK) && lane < k && sh.drafts[lane] != a;
+  const bool stop = (st == SPEC_OK) && lane < k && drafts[lane] != a;
   const uint32_t mask = __ballot_sync(0xFFFFFFFFu, stop);
   const int n = mask ? (__ffs(mask) - 1) : k;
   if (lane == 0) {
@@ -1366,7 +1393,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
         flags |= e.z;
       }
     }
-    greedy_finish(p, sh, b, k, off, status, key, __reduce_or_sync(0xFFFFFFFFu, flags), lane);
+    greedy_finish(p, sh.drafts, b, k, off, status, key, __reduce_or_sync(0xFFFFFFFFu, flags), lane);
     return;
   }
 
@@ -1455,6 +1482,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     if (lane == 0) {
       sh.scan_n = n;
       sh.scan_mode = (st == SPEC_OK) ? mode : kNoDraw;
+      if (st == SPEC_OK) draw_coef_store(sh.dcoef, sh.fin, (mode == kResidual) ? n : k, (mode == kResidual) ? n : -1, c);
       // The draw re-reads this CTA's slice of one row pair; on rounds larger
       // than L2 part of it may have left L2 since pass 1: fetch it back now.
       if (ALIGNED && st == SPEC_OK && body > 0) {
@@ -1528,28 +1556,13 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   auto seg_lsum = [&](int w) -> float* {
     return keep_rounds ? lane_sums + static_cast<int64_t>(w) * seg_rounds * 32 : nullptr;
   };
-  auto make_coef = [&]() {
-    DrawCoef kc;
-    const Partial pt = sh.fin[2 * draw_row];
-    kc.mp = scaled_ref(pt.m, c);
-    kc.l2sp = log2f(pt.s);
-    kc.c = c;
-    kc.mq = 0.f;
-    kc.l2sq = 0.f;
-    if (residual) {
-      const Partial pq = sh.fin[2 * n + 1];
-      kc.mq = scaled_ref(pq.m, c);
-      kc.l2sq = log2f(pq.s);
-    }
-    return kc;
-  };
 
   float W = 0.f;
   float resid_mass = NAN;
   int buf = 0;
   for (int attempt = 0; attempt < 2; ++attempt) {
     buf = attempt;
-    const DrawCoef kc = make_coef();
+    const DrawCoef kc = draw_coef_load(sh.dcoef);
     const uint8_t* trow = p.target + static_cast<int64_t>(off + draw_row) * p.ld_bytes;
     if (warp < kConsumerWarps) {
       const int s0 = v0 + warp * seg;
@@ -1588,6 +1601,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     // The residual max(0, p_n - q_n) has no mass: draw from p_n instead.
     residual = false;
     draw_row = n;
+    if (tid == 0) draw_coef_store(sh.dcoef, sh.fin, n, -1, c);
     __syncthreads();
   }
 
@@ -1634,7 +1648,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     if (fw < 0) fw = last_warp_with_weight();
   }
   if (fw >= 0 && warp == fw) {
-    const DrawCoef kc = make_coef();
+    const DrawCoef kc = draw_coef_load(sh.dcoef);
     const uint8_t* trow = p.target + static_cast<int64_t>(off + draw_row) * p.ld_bytes;
     const int s0 = v0 + warp * seg;
     const int s1 = min(v1, s0 + seg);
@@ -1654,6 +1668,103 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       }
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Small rounds
+// ---------------------------------------------------------------------------
+// Rounds without drafter logits whose rows are a few KB (every lane greedy;
+// a sampled lane reports SPEC_ERR_INVALID_ARG, as in the cluster kernel): one
+// CTA per lane, in which warp j reads row j with plain 16-byte loads, eight
+// in flight per lane, and reduces it in registers and shuffles -- no cluster,
+// ring or mbarrier, and every row of the lane in flight at once.  The row
+// keys (order-preserving max bits over the complemented index), the statuses
+// and the outputs are the cluster kernel's (argmax_key, greedy_finish), so
+// both give the same bits.
+constexpr int kSmallThreads = 32 * (kMaxDrafts + 1);
+constexpr int kSmallBatch = 8;  // vectors a lane loads before reducing them
+
+template <typename T, bool ALIGNED>
+__global__ void __launch_bounds__(kSmallThreads) verify_small_kernel(const VerifyParams p) {
+  constexpr int kVec = ElemTraits<T>::kVec;
+  __shared__ unsigned long long keys[kMaxDrafts + 1];
+  __shared__ uint32_t rflags[kMaxDrafts + 1];
+  __shared__ int drafts[kMaxDrafts + 1];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x;
+
+  // The lane metadata may be read before the wait for the previous kernel on
+  // the stream only when the caller says that kernel did not write it.
+  const bool meta_early = (p.flags & SPEC_VERIFY_META_BEFORE_WAIT) != 0u;
+  if (!meta_early) griddep_wait();
+  const int k = __ldg(p.draft_lens + b);
+  const int off = __ldg(p.row_offsets + b);
+  const int off_end = __ldg(p.row_offsets + b + 1);
+  const bool sampled = __ldg(p.temps + b) > 0.f;
+  int status = SPEC_OK;
+  if (k < 0 || off < 0 || off_end > p.rows || off_end - off != k + 1) {
+    status = SPEC_ERR_LAYOUT;
+  } else if (k > kMaxDrafts) {
+    status = SPEC_ERR_UNSUPPORTED;
+  } else if (sampled && p.draft == nullptr) {
+    status = SPEC_ERR_INVALID_ARG;
+  }
+  if (meta_early) griddep_wait();  // logits and outputs only after the previous kernel
+  if (tid == 0) griddep_launch_dependents();
+  const bool ok = (status == SPEC_OK) && !sampled;
+  if (ok && tid < k) drafts[tid] = __ldg(p.draft_tokens + off + tid);
+
+  if (ok && warp <= k) {
+    const uint8_t* row = p.target + static_cast<int64_t>(off + warp) * p.ld_bytes;
+    float m = -INFINITY;
+    int idx = INT_MAX;
+    uint32_t bad = 0;
+    // Elements in increasing index order per lane; a strictly larger value
+    // takes over, so each lane keeps its lowest index of its max.
+    auto take = [&](float x, int e) {
+      bad |= !(x <= FLT_MAX) ? 1u : 0u;
+      if (x > m) {
+        m = x;
+        idx = e;
+      }
+    };
+    int e0 = 0;
+    if (ALIGNED) {
+      const int nvec = p.V / kVec;
+      const uint4* rv = reinterpret_cast<const uint4*>(row);
+      for (int v0 = lane; v0 < nvec; v0 += 32 * kSmallBatch) {
+        uint4 x[kSmallBatch];
+#pragma unroll
+        for (int u = 0; u < kSmallBatch; ++u)
+          if (v0 + 32 * u < nvec) x[u] = __ldg(rv + v0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < kSmallBatch; ++u) {
+          if (v0 + 32 * u < nvec) {
+#pragma unroll
+            for (int t = 0; t < kVec; ++t) take(vec_elem<T>(x[u], t), (v0 + 32 * u) * kVec + t);
+          }
+        }
+      }
+      e0 = nvec * kVec;
+    }
+    for (int e = e0 + lane; e < p.V; e += 32) take(ElemTraits<T>::load(row, e), e);
+    // The warp's largest key: the high words first, then the low words among them.
+    const unsigned long long key = argmax_key(m, idx);
+    const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(key >> 32));
+    const uint32_t lo = __reduce_max_sync(0xFFFFFFFFu, (static_cast<uint32_t>(key >> 32) == hi)
+                                                           ? static_cast<uint32_t>(key) : 0u);
+    bad = __reduce_or_sync(0xFFFFFFFFu, bad);
+    if (lane == 0) {
+      keys[warp] = (static_cast<unsigned long long>(hi) << 32) | lo;
+      rflags[warp] = bad ? kBadValue : 0u;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  const bool has_row = ok && lane <= k;
+  const unsigned long long key = has_row ? keys[lane] : 0ull;
+  const uint32_t flags = __reduce_or_sync(0xFFFFFFFFu, has_row ? rflags[lane] : 0u);
+  greedy_finish(p, drafts, b, k, off, status, key, flags, lane);
 }
 
 }  // namespace specv

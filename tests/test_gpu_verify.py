@@ -415,14 +415,17 @@ def test_rounds_choose_their_kernel_build_by_shape():
     above the parallel-issue size).  Row slices streamed in several chunks take
     the groups-of-4 build with drafter logits (the 128-lane ragged round) and the
     16-warp build without (the 64-lane greedy round), as does the 1-lane round of
-    4 KB rows."""
+    4 KB rows when the small-round kernel is switched off; with it, that round
+    runs one CTA per lane."""
     s8 = sv.spec_verify_launch_shape(8, 64, 151936, torch.bfloat16, with_draft=True)
     g8 = sv.spec_verify_launch_shape(8, 64, 151936, torch.bfloat16, with_draft=False)
     s128 = sv.spec_verify_launch_shape(128, 563, 262144, torch.bfloat16, with_draft=True)
     g64 = sv.spec_verify_launch_shape(64, 256, 151936, torch.bfloat16, with_draft=False)
     g1 = sv.spec_verify_launch_shape(1, 4, 1024, torch.float32, with_draft=False)
     assert s8["threads"] == g8["threads"] == s128["threads"] == 22 * 32
-    assert g64["threads"] == g1["threads"] == 18 * 32
+    assert g64["threads"] == 18 * 32
+    # rows of at most 16 KB without drafter logits: the small-round kernel, one CTA of 16 warps per lane
+    assert (g1["cluster_ctas"], g1["threads"], g1["smem_bytes"]) == (1, 16 * 32, 0)
     # groups of five: eight 25 KB slots (over 200 KB); groups of four would hold five
     for s in (s8, g8):
         assert s["slice"] * 2 <= 40 * 1024 and s["smem_bytes"] > 8 * s["slice"] * 2
@@ -494,3 +497,68 @@ def test_lane_shards_reproduce_the_unsplit_round():
         torch.cuda.synchronize()
         assert np.array_equal(c.cpu().numpy(), full["committed"][lo:hi])
         assert np.array_equal(o.cpu().numpy(), full["out_tokens"][row_lo:row_hi])
+
+
+def _run_both_kernels(monkeypatch, r, stats):
+    small = run_gpu(r, stats=stats)
+    monkeypatch.setenv("SPEC_VERIFY_SMALL", "0")
+    cluster = run_gpu(r, stats=stats)
+    monkeypatch.delenv("SPEC_VERIFY_SMALL")
+    for key in small:
+        a, b = np.asarray(small[key]), np.asarray(cluster[key])
+        if a.dtype.kind == "f":
+            a, b = a.view(np.uint32 if a.itemsize == 4 else np.uint64), b.view(np.uint32 if b.itemsize == 4 else np.uint64)
+        np.testing.assert_array_equal(a, b, err_msg=key)
+    return small
+
+
+@pytest.mark.parametrize("stats", [True, False], ids=["stats", "nostats"])
+@pytest.mark.parametrize("dtype,vocab", [("bf16", 1), ("bf16", 7), ("f32", 8), ("f32", 9), ("bf16", 1023),
+                                         ("f32", 1024), ("f32", 4096), ("bf16", 4097), ("bf16", 8192)])
+def test_small_round_kernel_equals_the_cluster_kernel(monkeypatch, dtype, vocab, stats):
+    """Greedy rounds of rows up to 16 KB run one CTA per lane (one warp per
+    row, plain loads): every output, row statistics included, has the cluster
+    kernel's bits, and both match the oracle -- up to 16 rows a lane, ties
+    and ragged tails included."""
+    r = workloads.make_custom_round(70 + vocab, DEV, lanes=23, vocab=vocab, kmax=15, dtype=dtype, sampled="none")
+    # ties: a copy of each row's max a few elements later (the lowest index must win)
+    if vocab > 16:
+        t = r.target.float()
+        a = t.argmax(dim=1)
+        r.target[torch.arange(r.rows, device=DEV), (a + 5) % vocab] = r.target[torch.arange(r.rows, device=DEV), a]
+    shape = sv.spec_verify_launch_shape(r.lanes, r.rows, r.vocab, r.target.dtype)
+    assert (shape["cluster_ctas"], shape["threads"]) == (1, 16 * 32)
+    compare(r, _run_both_kernels(monkeypatch, r, stats), run_oracle(r), check_stats=stats)
+
+
+@pytest.mark.parametrize("layout", ["aligned", "padded", "misaligned"])
+def test_small_round_kernel_statuses_and_layouts(monkeypatch, layout):
+    """NaN, +inf and all -inf rows, draft tokens out of range, offsets that
+    disagree with the draft lengths, more drafts than supported and a sampled
+    lane without drafter logits: the small-round kernel reports what the
+    cluster kernel reports, on aligned, padded (element-wise) and misaligned rows."""
+    vocab = 1000
+    ld = vocab + 5 if layout == "padded" else None
+    r = workloads.make_custom_round(77, DEV, lanes=10, vocab=vocab, kmax=6, dtype="bf16", sampled="none",
+                                    fixed_k=True, ld=ld)
+    if layout == "misaligned":
+        t = r.target
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+        buf[1:] = t.reshape(-1)
+        r.target = buf[1:].view(t.shape)
+        assert r.target.data_ptr() % 16 != 0
+    off = r.row_offsets.cpu().numpy()
+    r.target[off[1] + 2, 7] = float("nan")
+    r.target[off[2] + 0, vocab - 3] = float("inf")
+    r.target[off[3] + 1, :vocab] = float("-inf")
+    r.target[off[4]:off[5], ::3] = float("-inf")   # allowed
+    r.draft_tokens[off[5] + 1] = vocab
+    r.draft_tokens[off[6]] = -1
+    r.temperatures[7] = 0.9                         # sampled, but no drafter logits
+    r.draft_lens[8] = 3                             # disagrees with the offsets
+    gpu = _run_both_kernels(monkeypatch, r, True)
+    assert gpu["lane_status"].tolist() == [0, 4, 4, 4, 0, 5, 5, 1, 6, 0]
+    compare(r, gpu, run_oracle(r))
+    r = workloads.make_custom_round(78, DEV, lanes=3, vocab=100, kmax=16, fixed_k=True, sampled="none")
+    gpu = _run_both_kernels(monkeypatch, r, False)
+    assert gpu["lane_status"].tolist() == [2, 2, 2] and (gpu["out_tokens"] == -1).all()
