@@ -119,6 +119,18 @@ __device__ __forceinline__ void bulk_s2g_hint(void* dst_gmem, const void* src_sm
       : "memory");
 }
 
+// 16-byte global -> shared copy by one thread (through L2 only), completed by
+// the same thread's cp.async.wait_group: each thread reads back only what it
+// copied itself, so no barrier is needed.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -776,16 +776,79 @@ __device__ __forceinline__ int warp_max_int(int v) {
 // elements; lane l holds elements 8l .. 8l+7 of each round.  `lsum`, when
 // given, keeps every lane's total of every round (lsum[r * 32 + lane]).
 
+// Builds that define SPEC_VERIFY_DRAW_STAGE stage the pass-2 rounds of long
+// segments (at least kDrawStageMinRounds full rounds) kDrawStage rounds ahead
+// in shared memory (cp.async, no registers held): the ragged 128-lane round,
+// 13 rounds a warp, 84.6 -> 83.9 us.  Compiled into the build that serves
+// the 8-lane sampled round (3 rounds a warp, never staged) the same code
+// cost that round 0.5 us, so only the build for streamed slices has it.
+#ifndef SPEC_VERIFY_DRAW_STAGE
+#define SPEC_VERIFY_DRAW_STAGE 0
+#endif
+constexpr bool kDrawStaged = SPEC_VERIFY_DRAW_STAGE != 0;
+constexpr int kDrawStage = 4;
+constexpr int kDrawStageMinRounds = 6;
+
+template <typename T>
+__host__ __device__ constexpr int draw_stage_bytes() {  // one warp's staging buffer
+  return kDrawStage * 64 * (ElemTraits<T>::kVec == 8 ? 16 : 32);
+}
+
 // Sum of the draw weights of the segment (every lane gets it).  Full rounds
-// run as packed pairs with the next half-batch's loads in flight; the last,
-// partial round is masked.
+// run as packed pairs, either staged through `stage` (a warp's
+// draw_stage_bytes of shared memory, or nullptr) or with the next
+// half-batch's loads in flight in registers; the last, partial round is
+// masked.
 template <typename T, bool ALIGNED, bool RESID>
 __device__ __forceinline__ float draw_segment_sum(const DrawCoef& kc, const uint8_t* trow, const uint8_t* qrow,
-                                                  int s0, int s1, float* lsum, int lane) {
+                                                  int s0, int s1, float* lsum, int lane, uint8_t* stage) {
   constexpr int kHalf = draw_batch<T>() / 2;
   const DrawCoef2 k2 = pack_coef(kc);
   const int nfull = (s1 > s0) ? (s1 - s0) / kDrawRound : 0;
   float acc = 0.f;
+  bool staged = false;
+  if constexpr (kDrawStaged) staged = ALIGNED && stage != nullptr && nfull >= kDrawStageMinRounds;
+  if (staged) {
+    // Round r of this lane sits at stage + (r mod kDrawStage) * 64 * LB + lane * LB
+    // (target) and 32 * LB further (drafter), LB = the bytes of eight elements.
+    constexpr int kLB = ElemTraits<T>::kVec == 8 ? 16 : 32;
+    constexpr int kEs = ElemTraits<T>::kVec == 8 ? 2 : 4;
+    uint8_t* mine = stage + lane * kLB;
+    auto issue = [&](int r) {
+      const int64_t src = static_cast<int64_t>(s0 + r * kDrawRound + lane * 8) * kEs;
+      uint8_t* dst = mine + (r % kDrawStage) * (64 * kLB);
+      cp_async16(dst, trow + src);
+      if constexpr (kLB == 32) cp_async16(dst + 16, trow + src + 16);
+      if constexpr (RESID) {
+        cp_async16(dst + 32 * kLB, qrow + src);
+        if constexpr (kLB == 32) cp_async16(dst + 32 * kLB + 16, qrow + src + 16);
+      }
+    };
+    // One commit group per round (empty past the end), so that waiting until
+    // at most kDrawStage - 1 groups are pending completes round r.
+#pragma unroll
+    for (int d = 0; d < kDrawStage - 1; ++d) {
+      issue(d);  // nfull >= kDrawStageMinRounds > kDrawStage - 1
+      cp_async_commit();
+    }
+    for (int r = 0; r < nfull; ++r) {
+      if (r + kDrawStage - 1 < nfull) issue(r + kDrawStage - 1);
+      cp_async_commit();
+      cp_async_wait<kDrawStage - 1>();
+      const uint8_t* src = mine + (r % kDrawStage) * (64 * kLB);
+      Raw8<T> rt, rq;
+      rt.v[0] = *reinterpret_cast<const uint4*>(src);
+      if constexpr (kLB == 32) rt.v[1] = *reinterpret_cast<const uint4*>(src + 16);
+      if constexpr (RESID) {
+        rq.v[0] = *reinterpret_cast<const uint4*>(src + 32 * kLB);
+        if constexpr (kLB == 32) rq.v[1] = *reinterpret_cast<const uint4*>(src + 32 * kLB + 16);
+      }
+      const float t = piece_total<T, RESID>(k2, rt, rq);
+      if (lsum) lsum[r * 32 + lane] = t;
+      acc = __fadd_rn(acc, t);
+    }
+    cp_async_wait<0>();
+  } else {
   Raw8<T> rtA[kHalf], rqA[kHalf], rtB[kHalf], rqB[kHalf];
   auto load_half = [&](Raw8<T> (&rt)[kHalf], Raw8<T> (&rq)[kHalf], int r0) {
 #pragma unroll
@@ -814,6 +877,7 @@ __device__ __forceinline__ float draw_segment_sum(const DrawCoef& kc, const uint
     if (r + kHalf >= nfull) break;
     if (r + 2 * kHalf < nfull) load_half(rtA, rqA, r + 2 * kHalf);
     sum_half(rtB, rqB, r + kHalf);
+  }
   }
   const int tb = s0 + nfull * kDrawRound;
   if (tb < s1) {
@@ -1556,6 +1620,15 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   auto seg_lsum = [&](int w) -> float* {
     return keep_rounds ? lane_sums + static_cast<int64_t>(w) * seg_rounds * 32 : nullptr;
   };
+  // Each consumer warp's staging buffer follows the kept lane totals.
+  const int64_t lsum_bytes =
+      keep_rounds ? (static_cast<int64_t>(seg_rounds) * kConsumerWarps * 32 * 4 + 127) / 128 * 128 : 0;
+  const bool stage_fits = kDrawStaged && ALIGNED &&
+                          lsum_bytes + static_cast<int64_t>(draw_stage_bytes<T>()) * kConsumerWarps <=
+                              static_cast<int64_t>(nslots) * p.slot_bytes;
+  uint8_t* const stage =
+      (stage_fits && warp < kConsumerWarps) ? ring + lsum_bytes + static_cast<int64_t>(draw_stage_bytes<T>()) * warp
+                                            : nullptr;
 
   float W = 0.f;
   float resid_mass = NAN;
@@ -1568,8 +1641,8 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       const int s0 = v0 + warp * seg;
       const int s1 = min(v1, s0 + seg);
       const float segw = residual
-                             ? draw_segment_sum<T, ALIGNED, true>(kc, trow, qrow, s0, s1, seg_lsum(warp), lane)
-                             : draw_segment_sum<T, ALIGNED, false>(kc, trow, qrow, s0, s1, seg_lsum(warp), lane);
+                             ? draw_segment_sum<T, ALIGNED, true>(kc, trow, qrow, s0, s1, seg_lsum(warp), lane, stage)
+                             : draw_segment_sum<T, ALIGNED, false>(kc, trow, qrow, s0, s1, seg_lsum(warp), lane, stage);
       if (lane == 0) sh.segsum[warp] = segw;
     }
     __syncthreads();
@@ -1709,10 +1782,10 @@ __global__ void __launch_bounds__(kSmallThreads) verify_small_kernel(const Verif
   } else if (sampled && p.draft == nullptr) {
     status = SPEC_ERR_INVALID_ARG;
   }
+  const bool ok = (status == SPEC_OK) && !sampled;
+  if (ok && tid < k) drafts[tid] = __ldg(p.draft_tokens + off + tid);  // lane metadata too
   if (meta_early) griddep_wait();  // logits and outputs only after the previous kernel
   if (tid == 0) griddep_launch_dependents();
-  const bool ok = (status == SPEC_OK) && !sampled;
-  if (ok && tid < k) drafts[tid] = __ldg(p.draft_tokens + off + tid);
 
   if (ok && warp <= k) {
     const uint8_t* row = p.target + static_cast<int64_t>(off + warp) * p.ld_bytes;

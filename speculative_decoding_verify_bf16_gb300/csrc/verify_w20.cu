@@ -4,7 +4,10 @@
 // rows stream better with 16.  spec_verify.cu launches this build for rounds
 // with drafter logits when the four-groups-of-five build (verify_w20p5.cu)
 // would not double-buffer, and the 16-warp build for rounds without them.
+// Its slices stream in several chunks, so its draw segments are long: it
+// stages them through shared memory (SPEC_VERIFY_DRAW_STAGE).
 #define SPEC_VERIFY_CONSUMER_WARPS 20
+#define SPEC_VERIFY_DRAW_STAGE 1
 #define specv specv_w20
 #include "verify_kernel.cuh"
 #undef specv

@@ -127,3 +127,14 @@ def test_cpu_baseline_times_a_sample_of_whole_lanes():
     r = workloads.make_custom_round(7, "cpu", lanes=6, vocab=500, kmax=5, dtype="bf16", sampled="mixed")
     line = bench.cpu_baseline("unused", 0, budget_s=0.2, gpu_round=r)
     assert line["kind"] == "oracle" and line["cores"] >= 1 and line["value"] > 0 and line["unit"] == "rows/s"
+
+
+def test_l2_note_states_whether_the_input_sets_leave_l2():
+    """Tiny rounds rotate over 16 sets that all stay in L2; the note says so
+    instead of claiming the sets leave L2 between reuses."""
+    b = object.__new__(bench.Bench)
+    b.sets, b.set_bytes = [None] * 16, 16440
+    assert "L2-resident" in b.l2_note()
+    b.sets, b.set_bytes = [None] * 2, 590_000_000
+    note = b.l2_note()
+    assert "more than the 129 MB L2" in note and "590 MB between reuses" in note
