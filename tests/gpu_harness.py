@@ -11,7 +11,8 @@ Tolerances (derived from the arithmetic; see the design notes):
   from p), i.e. where the oracle's draw lay within 1e-5 of a CDF boundary in
   normalised units;
 * exemptions (acceptance decisions or draws allowed to differ) are counted,
-  and a comparison fails if they exceed 1e-3 of its sampled lanes;
+  and a comparison fails if they exceed 1e-3 of its sampled lanes, rounded
+  up (so one in a comparison of fewer than 1000 sampled lanes);
 * log p(d), log q(d) and the log-sum-exp: within 1e-5 (absolute in log space,
   i.e. 1e-5 relative on the probabilities);
 * residual mass: within 1e-5 * W + 2e-6.
@@ -30,8 +31,9 @@ EXEMPT_FRAC = 1e-3
 
 
 def exemption_cap(sampled_lanes):
-    """Most exempted decisions one comparison accepts: 1e-3 of its sampled lanes."""
-    return int(EXEMPT_FRAC * sampled_lanes)
+    """Most exempted decisions one comparison accepts: 1e-3 of its sampled
+    lanes, rounded up (none without a sampled lane)."""
+    return int(np.ceil(EXEMPT_FRAC * sampled_lanes - 1e-9)) if sampled_lanes > 0 else 0
 
 
 def logits_to_numpy(t, vocab):
@@ -111,7 +113,8 @@ def compare(r, gpu, orc, check_stats=True, oracle_inputs=None):
     lens = r.draft_lens.cpu().numpy()
     temps = r.temperatures.cpu().numpy()
     np.testing.assert_array_equal(gpu["lane_status"], orc.lane_status, err_msg="lane_status")
-    counts = {"lanes": r.lanes, "sampled": int((temps > 0).sum()), "accept_flips": 0, "draw_flips": 0}
+    counts = {"lanes": r.lanes, "sampled": int((temps > 0).sum()), "accept_flips": 0, "draw_flips": 0,
+              "exempted": []}
     target = draft = None
     for b in range(r.lanes):
         k = int(lens[b])
@@ -134,6 +137,7 @@ def compare(r, gpu, orc, check_stats=True, oracle_inputs=None):
                 margin = dict(((kind, pos), m) for kind, pos, m in orc.margins[b])[("accept", j)]
                 assert margin < ACCEPT_TOL, (b, "acceptance differs", j, margin)
                 counts["accept_flips"] += 1
+                counts["exempted"].append(("accept", b, j, float(margin)))
             else:
                 np.testing.assert_array_equal(t_g[:n_g], t_o[:n_o])
                 if target is None:
@@ -144,6 +148,8 @@ def compare(r, gpu, orc, check_stats=True, oracle_inputs=None):
                 ok, wx = draw_is_valid(r, orc, b, n_g, int(t_g[n_g]), u_draw, target, draft)
                 assert ok, (b, "draw differs beyond tolerance", int(t_g[n_g]), int(t_o[n_o]), wx)
                 counts["draw_flips"] += 1
+                dm = dict(((kind, pos), m) for kind, pos, m in orc.margins[b]).get(("draw", n_o), float("nan"))
+                counts["exempted"].append(("draw", b, n_g, int(t_g[n_g]), int(t_o[n_o]), float(dm), float(wx)))
             assert (t_g[c_g:] == -1).all()
             continue
         assert c_g == c_o, (b, c_g, c_o)
