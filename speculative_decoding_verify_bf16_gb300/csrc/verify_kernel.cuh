@@ -1749,7 +1749,8 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
 // Rounds without drafter logits whose rows are a few KB (every lane greedy;
 // a sampled lane reports SPEC_ERR_INVALID_ARG, as in the cluster kernel): one
 // CTA per lane, in which warp j reads row j with plain 16-byte loads, eight
-// in flight per lane, and reduces it in registers and shuffles -- no cluster,
+// in flight per lane, and reduces each batch of eight as a tree in registers,
+// then the warp by shuffles -- no cluster,
 // ring or mbarrier, and every row of the lane in flight at once.  The row
 // keys (order-preserving max bits over the complemented index), the statuses
 // and the outputs are the cluster kernel's (argmax_key, greedy_finish), so
@@ -1805,17 +1806,45 @@ __global__ void __launch_bounds__(kSmallThreads) verify_small_kernel(const Verif
     if (ALIGNED) {
       const int nvec = p.V / kVec;
       const uint4* rv = reinterpret_cast<const uint4*>(row);
+      // A batch is reduced as a tree, not element by element: its max with
+      // NaN propagated (a NaN or +inf flags the row), then the lowest index
+      // holding that max; a batch takes over only with a strictly larger max,
+      // since earlier batches hold lower indices.  Vectors past the row read
+      // as -inf, which is never taken.
+      const uint32_t ninf = (kVec == 8) ? 0xFF80FF80u : 0xFF800000u;
       for (int v0 = lane; v0 < nvec; v0 += 32 * kSmallBatch) {
         uint4 x[kSmallBatch];
 #pragma unroll
         for (int u = 0; u < kSmallBatch; ++u)
-          if (v0 + 32 * u < nvec) x[u] = __ldg(rv + v0 + 32 * u);
+          x[u] = (v0 + 32 * u < nvec) ? __ldg(rv + v0 + 32 * u) : make_uint4(ninf, ninf, ninf, ninf);
+        float vm[kSmallBatch];
 #pragma unroll
         for (int u = 0; u < kSmallBatch; ++u) {
-          if (v0 + 32 * u < nvec) {
+          vm[u] = vec_elem<T>(x[u], 0);
 #pragma unroll
-            for (int t = 0; t < kVec; ++t) take(vec_elem<T>(x[u], t), (v0 + 32 * u) * kVec + t);
+          for (int t = 1; t < kVec; ++t) vm[u] = f32_max_nan(vm[u], vec_elem<T>(x[u], t));
+        }
+#pragma unroll
+        for (int w = kSmallBatch / 2; w > 0; w /= 2)
+#pragma unroll
+          for (int u = 0; u < w; ++u) vm[u] = f32_max_nan(vm[u], vm[u + w]);
+        const float mb = vm[0];
+        bad |= !(mb <= FLT_MAX) ? 1u : 0u;
+        if (mb > m) {
+          int vi[kSmallBatch];
+#pragma unroll
+          for (int u = 0; u < kSmallBatch; ++u) {
+            vi[u] = INT_MAX;
+#pragma unroll
+            for (int t = kVec - 1; t >= 0; --t)
+              if (vec_elem<T>(x[u], t) == mb) vi[u] = (v0 + 32 * u) * kVec + t;
           }
+#pragma unroll
+          for (int w = kSmallBatch / 2; w > 0; w /= 2)
+#pragma unroll
+            for (int u = 0; u < w; ++u) vi[u] = min(vi[u], vi[u + w]);
+          m = mb;
+          idx = vi[0];
         }
       }
       e0 = nvec * kVec;

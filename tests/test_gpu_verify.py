@@ -517,15 +517,19 @@ def _run_both_kernels(monkeypatch, r, stats):
                                          ("f32", 1024), ("f32", 4096), ("bf16", 4097), ("bf16", 8192)])
 def test_small_round_kernel_equals_the_cluster_kernel(monkeypatch, dtype, vocab, stats):
     """Greedy rounds of rows up to 16 KB run one CTA per lane (one warp per
-    row, plain loads): every output, row statistics included, has the cluster
-    kernel's bits, and both match the oracle -- up to 16 rows a lane, ties
-    and ragged tails included."""
+    row, plain loads, batches reduced as trees): every output, row statistics
+    included, has the cluster kernel's bits, and both match the oracle -- 1 to
+    16 rows a lane, ties within a batch and across batches, and ragged tails
+    included."""
     r = workloads.make_custom_round(70 + vocab, DEV, lanes=23, vocab=vocab, kmax=15, dtype=dtype, sampled="none")
-    # ties: a copy of each row's max a few elements later (the lowest index must win)
+    # ties: copies of each row's max a few elements later and a third of the
+    # row away, in another lane's vectors or batch (the lowest index must win)
     if vocab > 16:
         t = r.target.float()
         a = t.argmax(dim=1)
-        r.target[torch.arange(r.rows, device=DEV), (a + 5) % vocab] = r.target[torch.arange(r.rows, device=DEV), a]
+        rows = torch.arange(r.rows, device=DEV)
+        r.target[rows, (a + 5) % vocab] = r.target[rows, a]
+        r.target[rows, (a + vocab // 3) % vocab] = r.target[rows, a]
     shape = sv.spec_verify_launch_shape(r.lanes, r.rows, r.vocab, r.target.dtype)
     assert (shape["cluster_ctas"], shape["threads"]) == (1, 16 * 32)
     compare(r, _run_both_kernels(monkeypatch, r, stats), run_oracle(r), check_stats=stats)
