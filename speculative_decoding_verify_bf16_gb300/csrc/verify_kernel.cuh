@@ -1763,7 +1763,6 @@ __global__ void __launch_bounds__(kSmallThreads) verify_small_kernel(const Verif
   constexpr int kVec = ElemTraits<T>::kVec;
   __shared__ unsigned long long keys[kMaxDrafts + 1];
   __shared__ uint32_t rflags[kMaxDrafts + 1];
-  __shared__ int drafts[kMaxDrafts + 1];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x;
 
@@ -1784,7 +1783,9 @@ __global__ void __launch_bounds__(kSmallThreads) verify_small_kernel(const Verif
     status = SPEC_ERR_INVALID_ARG;
   }
   const bool ok = (status == SPEC_OK) && !sampled;
-  if (ok && tid < k) drafts[tid] = __ldg(p.draft_tokens + off + tid);  // lane metadata too
+  // Lane j of warp 0 holds draft j (lane metadata too) and checks its range.
+  const int draft = (ok && tid < k) ? __ldg(p.draft_tokens + off + tid) : 0;
+  const bool any_range_bad = __any_sync(0xFFFFFFFFu, ok && tid < k && (draft < 0 || draft >= p.V));
   if (meta_early) griddep_wait();  // logits and outputs only after the previous kernel
   if (tid == 0) griddep_launch_dependents();
 
@@ -1863,10 +1864,41 @@ __global__ void __launch_bounds__(kSmallThreads) verify_small_kernel(const Verif
   }
   __syncthreads();
   if (warp != 0) return;
+  // The acceptance scan and outputs, as greedy_finish writes them for the
+  // cluster kernel (no waits here, so no time-out), with the draft tokens
+  // already in registers.
   const bool has_row = ok && lane <= k;
   const unsigned long long key = has_row ? keys[lane] : 0ull;
-  const uint32_t flags = __reduce_or_sync(0xFFFFFFFFu, has_row ? rflags[lane] : 0u);
-  greedy_finish(p, drafts, b, k, off, status, key, flags, lane);
+  const bool nonfinite = __any_sync(0xFFFFFFFFu, has_row && (rflags[lane] != 0u || key == 0ull));
+  float m;
+  int a;
+  argmax_key_decode(key, m, a);
+  int st = status;
+  if (st == SPEC_OK) {
+    if (any_range_bad) st = SPEC_ERR_TOKEN_RANGE;
+    else if (nonfinite) st = SPEC_ERR_NONFINITE;
+  }
+  const uint32_t stops = __ballot_sync(0xFFFFFFFFu, ok && lane < k && draft != a);
+  const int n = (st != SPEC_OK) ? 0 : stops ? (__ffs(stops) - 1) : k;
+  if (lane == 0) {
+    p.committed[b] = (st == SPEC_OK) ? n + 1 : 0;
+    if (p.lane_status) p.lane_status[b] = st;
+  }
+  if (status == SPEC_ERR_LAYOUT) return;
+  for (int j = lane; j <= k; j += 32) {
+    p.out_tokens[off + j] = (st == SPEC_OK && j <= n) ? a : -1;
+    if (p.row_stats && st == SPEC_OK) {
+      spec_row_stats* rs = p.row_stats + off + j;
+      rs->argmax = a;
+      rs->max_logit = m;
+      rs->lse = NAN;
+      rs->logp_d = NAN;
+      rs->logq_d = NAN;
+      rs->resid_mass = NAN;
+      rs->drawn = -1;
+      rs->flags = 1;
+    }
+  }
 }
 
 }  // namespace specv
