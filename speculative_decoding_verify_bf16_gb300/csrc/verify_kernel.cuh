@@ -1228,6 +1228,11 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     const int j = sampled ? (s >> 1) : s;
     return (is_draft ? p.draft : p.target) + static_cast<int64_t>(off + j) * p.ld_bytes;
   };
+  // Pass 1 streams the rows last to first: the row pair most likely to be
+  // drawn from is the first rejected one, most often row 0, and streamed
+  // last it is the most likely still to be in L2 when the draw re-reads it.
+  // Position q of the pass-1 sequence is stream seq_stream(q).
+  auto seq_stream = [&](int q) { return nstreams - 1 - q; };
 
   // ---- pass 1 ----
   if (warp == kProducerWarp && p.slot_bytes <= kParallelIssueSlotBytes) {
@@ -1255,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
         }
         mbar_arrive_expect_tx(&sh.full[slot], static_cast<uint32_t>(L * kEsize));
         bulk_g2s(ring + static_cast<size_t>(slot) * p.slot_bytes,
-                 stream_row(s) + static_cast<int64_t>(v0 + c0) * kEsize, static_cast<uint32_t>(L * kEsize),
+                 stream_row(seq_stream(s)) + static_cast<int64_t>(v0 + c0) * kEsize, static_cast<uint32_t>(L * kEsize),
                  &sh.full[slot]);
         ++issued;
         ci += nprod;
@@ -1288,7 +1293,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       uint32_t it = 0;
       bool ok = true;
       for (int s = 0; s < nstreams && ok; ++s) {
-        const uint8_t* row = stream_row(s) + static_cast<int64_t>(v0) * kEsize;
+        const uint8_t* row = stream_row(seq_stream(s)) + static_cast<int64_t>(v0) * kEsize;
         for (int c0 = 0; c0 < body; c0 += slot_elems) {
           if (withhold_last && s == nstreams - 1 && c0 + slot_elems >= body) break;
           const int L = min(slot_elems, body - c0);
@@ -1357,9 +1362,9 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
           if (cur >= 0) {
             if (sampled) {
               const Partial wp = warp_merge<true>(a.m, a.s, a.idx, acc_bad(a), c);
-              if (lane == 0) sh.wpart[cur][warp] = wp;
+              if (lane == 0) sh.wpart[seq_stream(cur)][warp] = wp;
             } else {
-              fold_greedy_row(sh, cur, a.m, a.idx, acc_bad(a), lane);
+              fold_greedy_row(sh, seq_stream(cur), a.m, a.idx, acc_bad(a), lane);
             }
           }
           acc_init(a);
@@ -1394,9 +1399,9 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
         const uint32_t fl = acc_bad(a) | (ok ? 0u : kTimedOut);
         if (sampled) {
           const Partial wp = warp_merge<true>(a.m, a.s, a.idx, fl, c);
-          if (lane == 0) sh.wpart[cur][warp] = wp;
+          if (lane == 0) sh.wpart[seq_stream(cur)][warp] = wp;
         } else {
-          fold_greedy_row(sh, cur, a.m, a.idx, fl, lane);
+          fold_greedy_row(sh, seq_stream(cur), a.m, a.idx, fl, lane);
         }
       }
     }
