@@ -936,15 +936,57 @@ __device__ __noinline__ int draw_last_positive(const DrawCoef& kc, const uint8_t
 // lane totals, the element from the lane's own running sum; -2 if no round
 // crosses.  Where rounding leaves a round (or a lane) with no crossing
 // element, the last element of positive weight in it.  Whole warp.
+constexpr int kWalkSkipRounds = 8;
+
 template <typename T, bool ALIGNED, bool RESID>
 __device__ __noinline__ int draw_walk(const DrawCoef& kc, const uint8_t* trow, const uint8_t* qrow, int s0, int s1,
                                       const float* lsum, float tau, int lane) {
   const int nr = (s1 > s0) ? (s1 - s0 + kDrawRound - 1) / kDrawRound : 0;
   float run = 0.f;
   float w[8];
-  for (int r = 0; r < nr; ++r) {
+  int r0 = 0;  // first round to walk one by one
+  if (lsum && nr >= kWalkSkipRounds) {
+    // With the lane totals kept, long segments skip rounds 32 at a time (a
+    // few rounds are faster one by one): lane i sums
+    // the 32 lane totals of round rb + i (read in rotated order, one bank per
+    // lane), a prefix over the lanes gives the running totals, and a ballot
+    // finds the first round past tau.
+    for (int rb = 0; rb < nr; rb += 32) {
+      const int r = rb + lane;
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      if (r < nr) {
+        const float* lt = lsum + r * 32;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          a0 = __fadd_rn(a0, lt[(i + lane) & 31]);
+          a1 = __fadd_rn(a1, lt[(i + 1 + lane) & 31]);
+          a2 = __fadd_rn(a2, lt[(i + 2 + lane) & 31]);
+          a3 = __fadd_rn(a3, lt[(i + 3 + lane) & 31]);
+        }
+      }
+      float incl = __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3));
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float up = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl = __fadd_rn(up, incl);
+      }
+      const uint32_t past = __ballot_sync(0xFFFFFFFFu, r < nr && __fadd_rn(run, incl) > tau);
+      if (past) {
+        const int l = __ffs(past) - 1;
+        const float before = __shfl_sync(0xFFFFFFFFu, incl, (l > 0) ? l - 1 : 0);
+        if (l > 0) run = __fadd_rn(run, before);
+        r0 = rb + l;
+        break;
+      }
+      run = __fadd_rn(run, __shfl_sync(0xFFFFFFFFu, incl, 31));
+      r0 = min(nr, rb + 32);
+    }
+  }
+  for (int r = r0; r < nr; ++r) {
     const int base = s0 + r * kDrawRound;
     const float lt = lsum ? lsum[r * 32 + lane] : draw_round_weights<T, ALIGNED, RESID>(kc, trow, qrow, base, s1, lane, w);
+    // With kept totals, round r0 is the one found above; summed another way
+    // here it may fall short of tau by a rounding, and the walk goes on.
     const float next = __fadd_rn(run, warp_sum_xor(lt));
     if (next > tau) {
       if (lsum) draw_round_weights<T, ALIGNED, RESID>(kc, trow, qrow, base, s1, lane, w);
