@@ -370,9 +370,10 @@ __device__ __forceinline__ int vec_find(const uint4* sv, int vv, float m) {
 // the lane's running sum with one rescaling exp2.
 //
 // LAZY (sampled rows whose max and argmax are not reported): once the lane
-// has a finite reference M (the max of the groups taken so far), a group's
-// exponentials are summed against M directly, with no group max.  The sum of
-// 32 terms is at most 32 while no element exceeds M; a sum above 2^64, +inf
+// has a finite reference M (the max of the row's groups taken so far, carried
+// from piece to piece), a group's exponentials are summed against M
+// directly, with no group max.  The sum of 32 terms is at most 32 while no
+// element exceeds M; a sum above 2^64, +inf
 // or NaN sends the group through the exact path above instead, which raises
 // M, rescales, and flags NaN and +inf.  M then stays an element value at or
 // below the row max, and every later use of the partial (merges, the
@@ -390,6 +391,14 @@ __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int v
   float S = 0.f;  // sampled: sum relative to scaled_ref(M)
   float rM = 0.f; // LAZY: scaled_ref(M) while M is finite
   int gv = -1;    // first vector holding M
+  if constexpr (LAZY) {
+    // A piece continues the row's reference from the pieces before it, so
+    // that only a row's first group needs the exact path.
+    if (a.m != -INFINITY) {
+      M = a.m;
+      rM = scaled_ref(M, c);
+    }
+  }
   const unsigned long long c2 = f2_pack(c, c);
   // LAZY: the group's exponentials against the lane's reference.
   auto lazy_sum = [&](const uint4 (&x)[4]) -> float {
@@ -477,9 +486,13 @@ __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int v
   if (nanacc != nanacc || nanacc == INFINITY) a.bad = 1;
   if (M == -INFINITY) return;
   if (SAMPLED) {
-    // LAZY: any element index marks the partial as holding elements
-    const int e = LAZY ? ebase : (M >= a.m) ? ebase + vec_find<T>(sv, gv, M) : INT_MAX;
-    merge_part<true>(a.m, a.s, a.idx, M, S, e, c);
+    if (LAZY && M == a.m) {
+      a.s += S;  // the same reference: nothing to rescale
+    } else {
+      // LAZY: any element index marks the partial as holding elements
+      const int e = LAZY ? ebase : (M >= a.m) ? ebase + vec_find<T>(sv, gv, M) : INT_MAX;
+      merge_part<true>(a.m, a.s, a.idx, M, S, e, c);
+    }
   } else if (M > a.m) {
     acc_raise<false>(a, M, ebase + vec_find<T>(sv, gv, M), c);
   }
