@@ -450,6 +450,15 @@ __device__ __forceinline__ void acc_range(Acc& a, const uint4* sv, int vb, int v
   };
   int v = vb + lane;
   if constexpr (LAZY) {
+    // A row's first piece takes its reference from the lane's first element:
+    // any finite element value at or below the row max will do.
+    if (M == -INFINITY && v < ve) {
+      const float x0 = vec_elem<T>(sv[v], 0);
+      if (x0 > -INFINITY && x0 <= FLT_MAX) {
+        M = x0;
+        rM = scaled_ref(M, c);
+      }
+    }
     // A tight loop of lazily summed groups; a group it cannot take (no
     // reference yet, or a sum out of range) leaves it for the exact path,
     // which is kept out of the loop body.
