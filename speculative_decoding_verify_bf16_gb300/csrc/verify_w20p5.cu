@@ -8,6 +8,7 @@
 // rounds only with slots above 8 KB (the 8-lane greedy round: 6.36 -> 6.3 us).
 #define SPEC_VERIFY_CONSUMER_WARPS 20
 #define SPEC_VERIFY_PIECES 5
+#define SPEC_VERIFY_LAZY_VEC_TAIL 1
 #define specv specv_w20p5
 #include "verify_kernel.cuh"
 #undef specv
