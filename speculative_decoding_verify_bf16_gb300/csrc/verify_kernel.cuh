@@ -83,6 +83,7 @@ struct __align__(16) Partial {
 
 constexpr uint32_t kBadValue = 1u;  // NaN or +inf in the row
 constexpr uint32_t kTimedOut = 2u;  // a bounded wait gave up
+constexpr uint32_t kEmptyRow = 4u;  // a row with no finite logit (scan flags only)
 
 struct __align__(16) DrawPartial {
   float w;  // sum of draw weights over one CTA's slice
@@ -108,8 +109,15 @@ struct __align__(16) SmemHead {
   float xd_q[kMaxDrafts + 1];  // drafter logit at d_{j+1} in row j
   float u_acc[kMaxDrafts + 1];  // acceptance uniform of position j
   float u_smp[kMaxDrafts + 1];  // draw uniform of position j
+  float u_l2i[kMaxDrafts + 1];  // log2 of u_acc[j], split as log2_parts does
+  float u_l2f[kMaxDrafts + 1];
+  float scan_lp[kMaxDrafts + 1];  // sampled scan: log2 p_j(d), log2 q_j(d) (row statistics)
+  float scan_lq[kMaxDrafts + 1];
   int scan_n;
   int scan_mode;
+  int scan_st;            // sampled scan: the lane's status
+  int draft_range_bad;    // some draft token is outside [0, V)
+  uint32_t scan_flags;    // sampled lanes: OR of the merged rows' flags and kEmptyRow
   uint32_t cta_flags;
   int order_hist[kCostBuckets];  // lanes per cost class (longest-first lane order)
   int order_cnt[kWarps];
@@ -1251,6 +1259,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     mbar_init(&sh.dbar[0], 1);
     mbar_init(&sh.dbar[1], 1);
     sh.cta_flags = 0;
+    sh.scan_flags = 0;
     fence_mbar_init();
   }
   if (tid <= kMaxDrafts) sh.gkey[tid] = 0ull;
@@ -1424,8 +1433,17 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
         const float2 u = round_uniforms(p.seed, p.lane_base + static_cast<uint32_t>(b), static_cast<uint32_t>(j));
         sh.u_acc[j] = u.x;
         sh.u_smp[j] = u.y;
+        // The scan's log2(u), split ahead of time.
+        float iu = 0.f, fu = 0.f;
+        if (u.x != 0.f) log2_parts(u.x, iu, fu);
+        sh.u_l2i[j] = iu;
+        sh.u_l2f[j] = fu;
       }
     }
+    __syncwarp();
+    const bool range_bad = status == SPEC_OK && lane < k && (sh.drafts[lane] < 0 || sh.drafts[lane] >= p.V);
+    const bool any_bad = __any_sync(0xFFFFFFFFu, range_bad);
+    if (lane == 0) sh.draft_range_bad = any_bad ? 1 : 0;
   } else {
     // Consumer warps.  The work items are (chunk, piece): chunk ch of the ring
     // sequence is split into kPieces ranges of vectors, and warp w takes items
@@ -1577,34 +1595,27 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     for (int s = warp; s < nstreams; s += kConsumerWarps) {
       const Partial q = (lane < C) ? sh.cpart[lane][s] : identity_partial();
       const Partial r = warp_merge<true>(q.m, q.s, q.idx, q.flags, c);
-      if (lane == 0) sh.fin[s] = r;
+      if (lane == 0) {
+        sh.fin[s] = r;
+        const uint32_t f = r.flags | ((r.idx == INT_MAX) ? kEmptyRow : 0u);
+        if (f) atomicOr(&sh.scan_flags, f);
+      }
     }
   }
   __syncthreads();
 
   // ---- acceptance scan (warp 0; lane j handles position j) ----
+  // The draft range check, the split log2 of each uniform and the rows'
+  // flags are ready before it starts; each lane also forms the draw
+  // coefficients of its own rows, so that the chosen row's only need a
+  // shuffle once the scan knows it.
   if (warp == 0) {
     int st = status;
+    if (st == SPEC_OK && sh.draft_range_bad) st = SPEC_ERR_TOKEN_RANGE;
     if (st == SPEC_OK) {
-      bool range_bad = false;
-      if (lane < k) {
-        const int d = sh.drafts[lane];
-        range_bad = (d < 0 || d >= p.V);
-      }
-      if (__any_sync(0xFFFFFFFFu, range_bad)) st = SPEC_ERR_TOKEN_RANGE;
-    }
-    if (st == SPEC_OK) {
-      uint32_t fl = 0;
-      bool empty_row = false;
-      for (int s = lane; s < nstreams; s += 32) {
-        fl |= sh.fin[s].flags;
-        empty_row |= (sh.fin[s].idx == INT_MAX);
-      }
-      fl |= sh.cta_flags;
-      const uint32_t all = __reduce_or_sync(0xFFFFFFFFu, fl);
-      const bool any_empty = __any_sync(0xFFFFFFFFu, empty_row);
+      const uint32_t all = sh.scan_flags | sh.cta_flags;
       if (all & kTimedOut) st = SPEC_ERR_TIMEOUT;
-      else if ((all & kBadValue) || any_empty) st = SPEC_ERR_NONFINITE;
+      else if (all & (kBadValue | kEmptyRow)) st = SPEC_ERR_NONFINITE;
     }
 
     int n = 0, mode = kNoDraw;
@@ -1612,13 +1623,22 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     // log2(u) < log2 p - log2 q, as one compensated fp32 sum of exact terms:
     // its rounding error is far below the ~1e-6 relative error of the sums S.
     float lp = NAN, lq = NAN;
+    float cmp = 0.f, clp = 0.f, cmq = 0.f, clq = 0.f;  // this lane's rows' draw coefficients
     if (st == SPEC_OK) {
       const bool active = lane < k;
       bool accept = true;
+      if (lane <= k) {
+        const Partial pt = sh.fin[2 * lane];
+        cmp = scaled_ref(pt.m, c);
+        clp = log2f(pt.s);
+      }
       if (active) {
+        const Partial pq = sh.fin[2 * lane + 1];
+        cmq = scaled_ref(pq.m, c);
+        clq = log2f(pq.s);
         const float xt = sh.xd_t[lane], xq = sh.xd_q[lane];
         CompSum dp = log2_prob_terms(xt, sh.fin[2 * lane], c);
-        const CompSum dq = log2_prob_terms(xq, sh.fin[2 * lane + 1], c);
+        const CompSum dq = log2_prob_terms(xq, pq, c);
         lp = (xt == -INFINITY) ? -INFINITY : dp.value();
         lq = (xq == -INFINITY) ? -INFINITY : dq.value();
         const float u = sh.u_acc[lane];
@@ -1627,12 +1647,10 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
         } else if (xq == -INFINITY || u == 0.f) {
           accept = true;   // q(d) = 0, or log2(u) = -inf
         } else {
-          float iu, fu;
-          log2_parts(u, iu, fu);
           dp.add(-dq.s);
           dp.add(-dq.c);
-          dp.add(-iu);
-          dp.add(-fu);
+          dp.add(-sh.u_l2i[lane]);
+          dp.add(-sh.u_l2f[lane]);
           accept = dp.value() > 0.f;
         }
       }
@@ -1640,56 +1658,73 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       n = mask ? (__ffs(mask) - 1) : k;
       mode = (n < k) ? kResidual : kBonus;
     }
+    // The draw re-reads this CTA's slice of one row pair; on rounds larger
+    // than L2 part of it may have left L2 since pass 1: fetch it back now.
+    if (lane == 0 && ALIGNED && st == SPEC_OK && body > 0) {
+      const int drow = (mode == kResidual) ? n : k;
+      const int64_t col = static_cast<int64_t>(v0) * kEsize;
+      bulk_prefetch_l2(p.target + static_cast<int64_t>(off + drow) * p.ld_bytes + col,
+                       static_cast<uint32_t>(body * kEsize));
+      if (mode == kResidual)
+        bulk_prefetch_l2(p.draft + static_cast<int64_t>(off + n) * p.ld_bytes + col,
+                         static_cast<uint32_t>(body * kEsize));
+    }
+    const int src = (mode == kResidual) ? n : k;
+    const float mp = __shfl_sync(0xFFFFFFFFu, cmp, src & 31), l2sp = __shfl_sync(0xFFFFFFFFu, clp, src & 31);
+    const float mq = __shfl_sync(0xFFFFFFFFu, cmq, src & 31), l2sq = __shfl_sync(0xFFFFFFFFu, clq, src & 31);
     if (lane == 0) {
       sh.scan_n = n;
       sh.scan_mode = (st == SPEC_OK) ? mode : kNoDraw;
-      if (st == SPEC_OK) draw_coef_store(sh.dcoef, sh.fin, (mode == kResidual) ? n : k, (mode == kResidual) ? n : -1, c);
-      // The draw re-reads this CTA's slice of one row pair; on rounds larger
-      // than L2 part of it may have left L2 since pass 1: fetch it back now.
-      if (ALIGNED && st == SPEC_OK && body > 0) {
-        const int drow = (mode == kResidual) ? n : k;
-        const int64_t col = static_cast<int64_t>(v0) * kEsize;
-        bulk_prefetch_l2(p.target + static_cast<int64_t>(off + drow) * p.ld_bytes + col,
-                         static_cast<uint32_t>(body * kEsize));
-        if (mode == kResidual)
-          bulk_prefetch_l2(p.draft + static_cast<int64_t>(off + n) * p.ld_bytes + col,
-                           static_cast<uint32_t>(body * kEsize));
+      sh.scan_st = st;
+      if (st == SPEC_OK) {
+        // As draw_coef_store writes them for target row src (and drafter
+        // row n for a residual draw).
+        sh.dcoef[0] = mp;
+        sh.dcoef[1] = l2sp;
+        sh.dcoef[2] = (mode == kResidual) ? mq : 0.f;
+        sh.dcoef[3] = (mode == kResidual) ? l2sq : 0.f;
+        sh.dcoef[4] = c;
       }
     }
-
-    // ---- outputs (leader) ----
-    if (leader) {
-      const bool layout_ok = (status != SPEC_ERR_LAYOUT);
-      if (lane == 0) {
-        p.committed[b] = (st == SPEC_OK) ? n + 1 : 0;
-        if (p.lane_status) p.lane_status[b] = st;
-      }
-      for (int j = lane; layout_ok && j <= k; j += 32) {
-        const int tok = (st == SPEC_OK && j < n) ? sh.drafts[j] : -1;
-        const bool drawn_here = (st == SPEC_OK) && j == n;
-        if (!drawn_here) p.out_tokens[off + j] = tok;
-        if (p.row_stats && st == SPEC_OK) {
-          spec_row_stats* rs = p.row_stats + off + j;
-          const Partial pt = sh.fin[2 * j];
-          rs->argmax = pt.idx;
-          rs->max_logit = pt.m;
-          float ip, fp;
-          log2_parts(pt.s, ip, fp);
-          CompSum l;
-          l.add(scaled_ref(pt.m, c));
-          l.add(ip);
-          l.add(fp);
-          rs->lse = __fmul_rn(l.value(), kLn2);
-          rs->logp_d = (j < k) ? __fmul_rn(lp, kLn2) : NAN;
-          rs->logq_d = (j < k) ? __fmul_rn(lq, kLn2) : NAN;
-          if (!(drawn_here && mode == kResidual)) rs->resid_mass = NAN;
-          if (!drawn_here) rs->drawn = -1;
-          rs->flags = 1 | (drawn_here ? (mode == kResidual ? 2 : 4) : 0);
-        }
-      }
+    if (lane <= kMaxDrafts) {
+      sh.scan_lp[lane] = lp;
+      sh.scan_lq[lane] = lq;
     }
   }
   __syncthreads();
+
+  // ---- outputs (leader, by the helper warp, which has no part in the draw sums) ----
+  if (warp == kHelperWarp && leader) {
+    const int st = sh.scan_st, n = sh.scan_n, mode = sh.scan_mode;
+    const bool layout_ok = (status != SPEC_ERR_LAYOUT);
+    if (lane == 0) {
+      p.committed[b] = (st == SPEC_OK) ? n + 1 : 0;
+      if (p.lane_status) p.lane_status[b] = st;
+    }
+    for (int j = lane; layout_ok && j <= k; j += 32) {
+      const int tok = (st == SPEC_OK && j < n) ? sh.drafts[j] : -1;
+      const bool drawn_here = (st == SPEC_OK) && j == n;
+      if (!drawn_here) p.out_tokens[off + j] = tok;
+      if (p.row_stats && st == SPEC_OK) {
+        spec_row_stats* rs = p.row_stats + off + j;
+        const Partial pt = sh.fin[2 * j];
+        rs->argmax = pt.idx;
+        rs->max_logit = pt.m;
+        float ip, fp;
+        log2_parts(pt.s, ip, fp);
+        CompSum l;
+        l.add(scaled_ref(pt.m, c));
+        l.add(ip);
+        l.add(fp);
+        rs->lse = __fmul_rn(l.value(), kLn2);
+        rs->logp_d = (j < k) ? __fmul_rn(sh.scan_lp[j], kLn2) : NAN;
+        rs->logq_d = (j < k) ? __fmul_rn(sh.scan_lq[j], kLn2) : NAN;
+        if (!(drawn_here && mode == kResidual)) rs->resid_mass = NAN;
+        if (!drawn_here) rs->drawn = -1;
+        rs->flags = 1 | (drawn_here ? (mode == kResidual ? 2 : 4) : 0);
+      }
+    }
+  }
 
   if (sh.scan_mode == kNoDraw) return;
 
