@@ -968,7 +968,7 @@ __device__ __forceinline__ float draw_round_weights(const DrawCoef& kc, const ui
 // Largest index of positive weight in the segment (-1 if none): the last
 // round, then the last lane, holding weight.  Whole warp.
 template <typename T, bool ALIGNED, bool RESID>
-__device__ __noinline__ int draw_last_positive(const DrawCoef& kc, const uint8_t* trow, const uint8_t* qrow, int s0,
+__device__ __noinline__ int draw_last_positive(const DrawCoef kc, const uint8_t* trow, const uint8_t* qrow, int s0,
                                                int s1, const float* lsum, int lane) {
   const int nr = (s1 > s0) ? (s1 - s0 + kDrawRound - 1) / kDrawRound : 0;
   float w[8];
@@ -997,7 +997,7 @@ __device__ __noinline__ int draw_last_positive(const DrawCoef& kc, const uint8_t
 constexpr int kWalkSkipRounds = 8;
 
 template <typename T, bool ALIGNED, bool RESID>
-__device__ __noinline__ int draw_walk(const DrawCoef& kc, const uint8_t* trow, const uint8_t* qrow, int s0, int s1,
+__device__ __noinline__ int draw_walk(const DrawCoef kc, const uint8_t* trow, const uint8_t* qrow, int s0, int s1,
                                       const float* lsum, float tau, int lane) {
   const int nr = (s1 > s0) ? (s1 - s0 + kDrawRound - 1) / kDrawRound : 0;
   float run = 0.f;
@@ -1047,7 +1047,14 @@ __device__ __noinline__ int draw_walk(const DrawCoef& kc, const uint8_t* trow, c
     // here it may fall short of tau by a rounding, and the walk goes on.
     const float next = __fadd_rn(run, warp_sum_xor(lt));
     if (next > tau) {
-      if (lsum) draw_round_weights<T, ALIGNED, RESID>(kc, trow, qrow, base, s1, lane, w);
+      // With kept totals the round's elements are read again here: the
+      // loads go out first, and the lane is found from the kept totals while
+      // they are in flight.
+      Raw8<T> rt, rq;
+      if (lsum) {
+        load_raw8<T, ALIGNED>(trow, base + lane * 8, s1, rt);
+        if constexpr (RESID) load_raw8<T, ALIGNED>(qrow, base + lane * 8, s1, rq);
+      }
       const float tau2 = __fsub_rn(tau, run);
       float incl = lt;
 #pragma unroll
@@ -1061,6 +1068,7 @@ __device__ __noinline__ int draw_walk(const DrawCoef& kc, const uint8_t* trow, c
       const uint32_t pos_lanes = __ballot_sync(0xFFFFFFFFu, lt > 0.f);
       const int l = hit ? (__ffs(hit) - 1) : (pos_lanes ? 31 - __clz(pos_lanes) : 0);
       const float tau3 = __fsub_rn(tau2, excl);
+      if (lsum) piece_weights<T, RESID>(kc, rt, rq, base + lane * 8, s1, w);
       int t = -1, lastpos = -1;
       float cum = 0.f;
 #pragma unroll
@@ -1839,18 +1847,24 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       if (sh.dpart[buf][r].w > 0.f) last_r = r;
     if (last_r == static_cast<int>(rank)) fw = last_warp_with_weight();
   } else if (owner == static_cast<int>(rank)) {
+    // The warp segments' running totals by one scan across the lanes (lane w
+    // holds warp w's sum), the first past tau by a ballot.
     const float tau = __fsub_rn(target, prefix);
-    float q = 0.f;
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float next = __fadd_rn(q, sh.segsum[w]);
-      if (next > tau) {
-        fw = w;
-        tau_w = __fsub_rn(tau, q);
-        break;
-      }
-      q = next;
+    const float sw = (lane < kConsumerWarps) ? sh.segsum[lane] : 0.f;
+    float incl = sw;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float up = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl = __fadd_rn(up, incl);
     }
-    if (fw < 0) fw = last_warp_with_weight();
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, lane < kConsumerWarps && incl > tau);
+    const float before = __shfl_sync(0xFFFFFFFFu, incl, hit ? max(__ffs(hit) - 2, 0) : 0);
+    if (hit) {
+      fw = __ffs(hit) - 1;
+      tau_w = (fw > 0) ? __fsub_rn(tau, before) : tau;
+    } else {
+      fw = last_warp_with_weight();
+    }
   }
   if (fw >= 0 && warp == fw) {
     const DrawCoef kc = draw_coef_load(sh.dcoef);
