@@ -994,7 +994,10 @@ __device__ __noinline__ int draw_last_positive(const DrawCoef kc, const uint8_t*
 // lane totals, the element from the lane's own running sum; -2 if no round
 // crosses.  Where rounding leaves a round (or a lane) with no crossing
 // element, the last element of positive weight in it.  Whole warp.
-constexpr int kWalkSkipRounds = 8;
+#ifndef SPEC_VERIFY_WALK_SKIP_MIN
+#define SPEC_VERIFY_WALK_SKIP_MIN 2
+#endif
+constexpr int kWalkSkipRounds = SPEC_VERIFY_WALK_SKIP_MIN;
 
 template <typename T, bool ALIGNED, bool RESID>
 __device__ __noinline__ int draw_walk(const DrawCoef kc, const uint8_t* trow, const uint8_t* qrow, int s0, int s1,
@@ -1003,23 +1006,26 @@ __device__ __noinline__ int draw_walk(const DrawCoef kc, const uint8_t* trow, co
   float run = 0.f;
   float w[8];
   int r0 = 0;  // first round to walk one by one
+  float skip_next = -1.f;  // the running total through round r0, when the skip found it
   if (lsum && nr >= kWalkSkipRounds) {
     // With the lane totals kept, long segments skip rounds 32 at a time (a
-    // few rounds are faster one by one): lane i sums
-    // the 32 lane totals of round rb + i (read in rotated order, one bank per
-    // lane), a prefix over the lanes gives the running totals, and a ballot
-    // finds the first round past tau.
+    // few rounds are faster one by one): lane i sums the 32 lane totals of
+    // round rb + i, a prefix over the lanes gives the running totals, and a
+    // ballot finds the first round past tau.
     for (int rb = 0; rb < nr; rb += 32) {
       const int r = rb + lane;
       float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
       if (r < nr) {
-        const float* lt = lsum + r * 32;
+        // Eight 16-byte loads a lane, rotated so that each quarter-warp's
+        // eight lanes read eight different bank groups.
+        const float4* lt = reinterpret_cast<const float4*>(lsum + r * 32);
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          a0 = __fadd_rn(a0, lt[(i + lane) & 31]);
-          a1 = __fadd_rn(a1, lt[(i + 1 + lane) & 31]);
-          a2 = __fadd_rn(a2, lt[(i + 2 + lane) & 31]);
-          a3 = __fadd_rn(a3, lt[(i + 3 + lane) & 31]);
+        for (int i = 0; i < 8; ++i) {
+          const float4 q4 = lt[(i + lane) & 7];
+          a0 = __fadd_rn(a0, q4.x);
+          a1 = __fadd_rn(a1, q4.y);
+          a2 = __fadd_rn(a2, q4.z);
+          a3 = __fadd_rn(a3, q4.w);
         }
       }
       float incl = __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3));
@@ -1032,6 +1038,8 @@ __device__ __noinline__ int draw_walk(const DrawCoef kc, const uint8_t* trow, co
       if (past) {
         const int l = __ffs(past) - 1;
         const float before = __shfl_sync(0xFFFFFFFFu, incl, (l > 0) ? l - 1 : 0);
+        const float through = __shfl_sync(0xFFFFFFFFu, incl, l);
+        skip_next = __fadd_rn(run, through);  // past tau: round r0 crosses
         if (l > 0) run = __fadd_rn(run, before);
         r0 = rb + l;
         break;
@@ -1043,9 +1051,10 @@ __device__ __noinline__ int draw_walk(const DrawCoef kc, const uint8_t* trow, co
   for (int r = r0; r < nr; ++r) {
     const int base = s0 + r * kDrawRound;
     const float lt = lsum ? lsum[r * 32 + lane] : draw_round_weights<T, ALIGNED, RESID>(kc, trow, qrow, base, s1, lane, w);
-    // With kept totals, round r0 is the one found above; summed another way
-    // here it may fall short of tau by a rounding, and the walk goes on.
-    const float next = __fadd_rn(run, warp_sum_xor(lt));
+    // Round r0, when the skip found it, crosses by construction; its lanes'
+    // own scan below may then fall short by a rounding, which takes the
+    // last positive weight of the round.
+    const float next = (r == r0 && skip_next >= 0.f) ? skip_next : __fadd_rn(run, warp_sum_xor(lt));
     if (next > tau) {
       // With kept totals the round's elements are read again here: the
       // loads go out first, and the lane is found from the kept totals while
@@ -1772,6 +1781,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
 
   float W = 0.f;
   float resid_mass = NAN;
+  float dsum = 0.f, dincl = 0.f;  // lane r: CTA r's draw sum, and the running total through CTA r
   int buf = 0;
   for (int attempt = 0; attempt < 2; ++attempt) {
     buf = attempt;
@@ -1807,8 +1817,14 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     }
     __syncthreads();
 
-    W = 0.f;
-    for (int r = 0; r < C; ++r) W = __fadd_rn(W, sh.dpart[buf][r].w);
+    dsum = (lane < C) ? sh.dpart[buf][lane].w : 0.f;
+    dincl = dsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float up = __shfl_up_sync(0xFFFFFFFFu, dincl, o);
+      if (lane >= o) dincl = __fadd_rn(up, dincl);
+    }
+    W = __shfl_sync(0xFFFFFFFFu, dincl, C - 1);
     if (residual) resid_mass = W;
     if (W > 0.f || !residual) break;
     // The residual max(0, p_n - q_n) has no mass: draw from p_n instead.
@@ -1823,16 +1839,10 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   // crossing, the last element of positive weight (in the last CTA, and
   // then the last warp, holding weight).
   const float target = __fmul_rn(uprime, W);
-  int owner = -1;
-  float prefix = 0.f;
-  for (int r = 0; r < C; ++r) {
-    const float next = __fadd_rn(prefix, sh.dpart[buf][r].w);
-    if (next > target) {
-      owner = r;
-      break;
-    }
-    prefix = next;
-  }
+  const uint32_t cta_past = __ballot_sync(0xFFFFFFFFu, lane < C && dincl > target);
+  const int owner = cta_past ? (__ffs(cta_past) - 1) : -1;
+  const float prefix_l = __shfl_sync(0xFFFFFFFFu, dincl, (owner > 0) ? owner - 1 : 0);
+  const float prefix = (owner > 0) ? prefix_l : 0.f;
   auto last_warp_with_weight = [&]() {
     int lw = -1;
     for (int w = 0; w < kConsumerWarps; ++w)
@@ -1842,9 +1852,8 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
   int fw = -1;         // the warp that finds the token in this CTA
   float tau_w = -1.f;  // its threshold within its segment (< 0: the last positive weight)
   if (owner < 0) {
-    int last_r = -1;
-    for (int r = 0; r < C; ++r)
-      if (sh.dpart[buf][r].w > 0.f) last_r = r;
+    const uint32_t pos = __ballot_sync(0xFFFFFFFFu, lane < C && dsum > 0.f);
+    const int last_r = pos ? (31 - __clz(pos)) : -1;
     if (last_r == static_cast<int>(rank)) fw = last_warp_with_weight();
   } else if (owner == static_cast<int>(rank)) {
     // The warp segments' running totals by one scan across the lanes (lane w
