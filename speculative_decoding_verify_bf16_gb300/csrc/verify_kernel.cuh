@@ -1796,12 +1796,19 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       if (lane == 0) sh.segsum[warp] = segw;
     }
     __syncthreads();
-    if (tid < C) {
-      float wc = 0.f;
-      for (int w = 0; w < kConsumerWarps; ++w) wc = __fadd_rn(wc, sh.segsum[w]);
+    if (warp == 0) {
+      // The CTA's sum by the same scan across the lanes (lane w: warp w's
+      // segment) that later picks the walking warp, so the two agree.
+      float wc = (lane < kConsumerWarps) ? sh.segsum[lane] : 0.f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float up = __shfl_up_sync(0xFFFFFFFFu, wc, o);
+        if (lane >= o) wc = __fadd_rn(up, wc);
+      }
+      wc = __shfl_sync(0xFFFFFFFFu, wc, kConsumerWarps - 1);
       if (tid == static_cast<int>(rank)) {
         sh.dpart[buf][rank] = DrawPartial{wc, 0, 0, 0};
-      } else {
+      } else if (tid < C) {
         st_async_v4(cluster_map(&sh.dpart[buf][rank], tid), __float_as_uint(wc), 0u, 0u, 0u,
                     cluster_map(&sh.dbar[buf], tid));
       }
