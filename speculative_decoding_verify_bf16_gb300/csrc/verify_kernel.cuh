@@ -647,16 +647,21 @@ __device__ __forceinline__ CompSum log2_prob_terms(float xd, const Partial& row,
 // ---------------------------------------------------------------------------
 // Pass-2 draw weights
 // ---------------------------------------------------------------------------
-// The weight of element x is p(x) for a bonus draw and max(0, p(x) - q(x)) for
-// a residual draw, with p(x) = 2^(fl(fl(x * c - fl(m_p * c)) - log2 S_p)) and
-// q the same over the drafter row.  The sums take the weights as packed pairs
-// and the walk as scalars; both round every step identically, so each weight
-// has the same bits wherever it is formed, and a lane's eight weights are
-// always added in the same order (tree8).
+// A draw needs its weights only up to a common factor, so they are taken
+// times S_p, the target row's sum: the weight of element x is
+// p'(x) = 2^(fl(x * c - fl(m_p * c))) for a bonus draw and max(0, p'(x) -
+// q'(x)) for a residual draw, q'(x) = 2^(fl(fl(x * c - fl(m_q * c)) + e)) over
+// the drafter row with e = fl(log2 S_p - log2 S_q) (q(x) * S_p).  A bonus
+// weight is one FMA and one exp2.  The residual mass is the weights' total
+// times 2^(-log2 S_p).  The sums take the weights as packed pairs and the walk
+// as scalars; both round every step identically, so each weight has the same
+// bits wherever it is formed, and a lane's eight weights are always added in
+// the same order (tree8).
 struct DrawCoef {
-  float mp, l2sp;  // target row: scaled reference fl(max * c) and log2 of its sum
-  float mq, l2sq;  // drafter row (residual only)
-  float c;         // log2(e) / T
+  float mp;  // target row: scaled reference fl(max * c)
+  float mq;  // drafter row (residual only): its scaled reference
+  float e;   // fl(log2 S_p - log2 S_q) (residual only)
+  float c;   // log2(e) / T
 };
 
 // Coefficients of the weights of a draw from target row `rt` (and drafter row
@@ -678,45 +683,43 @@ __device__ __forceinline__ void draw_coef_store(float* out, const Partial* fin, 
 __device__ __forceinline__ DrawCoef draw_coef_load(const float* in) {
   DrawCoef k;
   k.mp = in[0];
-  k.l2sp = in[1];
   k.mq = in[2];
-  k.l2sq = in[3];
+  k.e = __fsub_rn(in[1], in[3]);
   k.c = in[4];
   return k;
 }
 
 template <bool RESID>
 __device__ __forceinline__ float draw_weight(const DrawCoef& k, float xt, float xq) {
-  const float p = ex2_approx(__fsub_rn(__fmaf_rn(xt, k.c, -k.mp), k.l2sp));
+  const float p = ex2_approx(__fmaf_rn(xt, k.c, -k.mp));
   if (!RESID) return p;
-  const float q = ex2_approx(__fsub_rn(__fmaf_rn(xq, k.c, -k.mq), k.l2sq));
+  const float q = ex2_approx(__fadd_rn(__fmaf_rn(xq, k.c, -k.mq), k.e));
   return fmaxf(0.f, __fsub_rn(p, q));
 }
 
 // The coefficients duplicated into packed pairs.
 struct DrawCoef2 {
-  unsigned long long c, nmp, nl2sp, nmq, nl2sq, neg1;
+  unsigned long long c, nmp, nmq, e, neg1;
 };
 
 __device__ __forceinline__ DrawCoef2 pack_coef(const DrawCoef& k) {
   DrawCoef2 r;
   r.c = f2_pack(k.c, k.c);
   r.nmp = f2_pack(-k.mp, -k.mp);
-  r.nl2sp = f2_pack(-k.l2sp, -k.l2sp);
   r.nmq = f2_pack(-k.mq, -k.mq);
-  r.nl2sq = f2_pack(-k.l2sq, -k.l2sq);
+  r.e = f2_pack(k.e, k.e);
   r.neg1 = f2_pack(-1.f, -1.f);
   return r;
 }
 
-// draw_weight of two elements at once: x - l2s is added as x + (-l2s), and
-// p - q formed as fma(q, -1, p), both rounded once, as the scalar forms are.
+// draw_weight of two elements at once: p' - q' is formed as fma(q', -1, p'),
+// rounded once, as the scalar form is.
 template <bool RESID>
 __device__ __forceinline__ unsigned long long draw_weight2(const DrawCoef2& k, unsigned long long xt,
                                                            unsigned long long xq) {
-  const unsigned long long p = f2_ex2(f2_add(f2_fma(xt, k.c, k.nmp), k.nl2sp));
+  const unsigned long long p = f2_ex2(f2_fma(xt, k.c, k.nmp));
   if (!RESID) return p;
-  const unsigned long long q = f2_ex2(f2_add(f2_fma(xq, k.c, k.nmq), k.nl2sq));
+  const unsigned long long q = f2_ex2(f2_add(f2_fma(xq, k.c, k.nmq), k.e));
   float lo, hi;
   f2_unpack(f2_fma(q, k.neg1, p), lo, hi);
   return f2_pack(fmaxf(0.f, lo), fmaxf(0.f, hi));
@@ -1832,7 +1835,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
       if (lane >= o) dincl = __fadd_rn(up, dincl);
     }
     W = __shfl_sync(0xFFFFFFFFu, dincl, C - 1);
-    if (residual) resid_mass = W;
+    if (residual) resid_mass = __fmul_rn(W, ex2_approx(-sh.dcoef[1]));  // W / S_p
     if (W > 0.f || !residual) break;
     // The residual max(0, p_n - q_n) has no mass: draw from p_n instead.
     residual = false;
