@@ -992,15 +992,18 @@ __device__ __noinline__ int draw_last_positive(const DrawCoef kc, const uint8_t*
   return -1;
 }
 
+// Segments of at least this many rounds find their crossing round 32 rounds
+// at a time (see draw_walk); shorter ones round by round.
+#ifndef SPEC_VERIFY_WALK_SKIP_MIN
+#define SPEC_VERIFY_WALK_SKIP_MIN 2
+#endif
+constexpr int kWalkSkipRounds = SPEC_VERIFY_WALK_SKIP_MIN;
+
 // Index of the element at which the running weight sum of the segment first
 // exceeds tau: the round from the round totals, the lane from a scan of the
 // lane totals, the element from the lane's own running sum; -2 if no round
 // crosses.  Where rounding leaves a round (or a lane) with no crossing
 // element, the last element of positive weight in it.  Whole warp.
-#ifndef SPEC_VERIFY_WALK_SKIP_MIN
-#define SPEC_VERIFY_WALK_SKIP_MIN 2
-#endif
-constexpr int kWalkSkipRounds = SPEC_VERIFY_WALK_SKIP_MIN;
 
 template <typename T, bool ALIGNED, bool RESID>
 __device__ __noinline__ int draw_walk(const DrawCoef kc, const uint8_t* trow, const uint8_t* qrow, int s0, int s1,
@@ -1844,10 +1847,10 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
     __syncthreads();
   }
 
-  // The CTA holding the crossing of u' * W (cumulative sums in CTA order),
-  // and in it the warp whose segment holds it; where rounding leaves no
-  // crossing, the last element of positive weight (in the last CTA, and
-  // then the last warp, holding weight).
+  // The CTA holding the crossing of u' * W (cumulative sums in CTA order, by
+  // the scan across the lanes above), and in it the warp whose segment holds
+  // it; where rounding leaves no crossing, the last element of positive
+  // weight (in the last CTA, and then the last warp, holding weight).
   const float target = __fmul_rn(uprime, W);
   const uint32_t cta_past = __ballot_sync(0xFFFFFFFFu, lane < C && dincl > target);
   const int owner = cta_past ? (__ffs(cta_past) - 1) : -1;
