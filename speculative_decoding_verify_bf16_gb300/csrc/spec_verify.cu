@@ -127,10 +127,14 @@ KernelVariant w16_variant() {
   v.groups = specv::kGroups;
   v.head_bytes_raw = static_cast<int>(sizeof(specv::SmemHead));
   v.consumer_warps = specv::kConsumerWarps;
-  v.kernel[0] = reinterpret_cast<void*>(&specv::verify_accept_kernel<float, false>);
-  v.kernel[1] = reinterpret_cast<void*>(&specv::verify_accept_kernel<float, true>);
-  v.kernel[2] = reinterpret_cast<void*>(&specv::verify_accept_kernel<bf16_tag, false>);
-  v.kernel[3] = reinterpret_cast<void*>(&specv::verify_accept_kernel<bf16_tag, true>);
+  v.kernel[0] = reinterpret_cast<void*>(&specv::verify_accept_kernel<float, false, false>);
+  v.kernel[1] = reinterpret_cast<void*>(&specv::verify_accept_kernel<float, true, false>);
+  v.kernel[2] = reinterpret_cast<void*>(&specv::verify_accept_kernel<bf16_tag, false, false>);
+  v.kernel[3] = reinterpret_cast<void*>(&specv::verify_accept_kernel<bf16_tag, true, false>);
+  v.kernel_exact[0] = reinterpret_cast<void*>(&specv::verify_accept_kernel<float, false, true>);
+  v.kernel_exact[1] = reinterpret_cast<void*>(&specv::verify_accept_kernel<float, true, true>);
+  v.kernel_exact[2] = reinterpret_cast<void*>(&specv::verify_accept_kernel<bf16_tag, false, true>);
+  v.kernel_exact[3] = reinterpret_cast<void*>(&specv::verify_accept_kernel<bf16_tag, true, true>);
   return v;
 }
 
@@ -258,10 +262,12 @@ int resolve_shape(DeviceCache* dc, int dev, int which, int lanes, int rows, int 
     std::lock_guard<std::mutex> lock(g_mutex);
     bool& done = dc->verify_attr[which * 4 + kernel_index(dtype, aligned)];
     if (!done) {
-      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dc->smem_optin) !=
-              cudaSuccess ||
-          cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-        return SPEC_ERR_CUDA;
+      // Both instantiations (lazy sweep and row statistics) share the shape.
+      for (void* k : {kernel, kv.kernel_exact[kernel_index(dtype, aligned)]}) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dc->smem_optin) != cudaSuccess ||
+            cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+          return SPEC_ERR_CUDA;
+      }
       done = true;
     }
   }
@@ -438,6 +444,8 @@ int spec_verify_accept(const spec_verify_args* a, void* stream) {
   const int rc = resolve_launch(dc, dev, a->draft_logits != nullptr, a->lanes, a->rows, a->V, a->dtype, aligned, &s,
                                 &kernel, &which);
   if (rc != SPEC_OK) return rc;
+  // Row statistics need the exact sweep's instantiation (same shape).
+  if (a->row_stats) kernel = variant(which).kernel_exact[kernel_index(a->dtype, aligned)];
 
   specv::VerifyParams p{};
   p.target = static_cast<const uint8_t*>(a->target_logits);

@@ -1252,7 +1252,10 @@ __device__ int lane_of_rank(const VerifyParams& p, SmemHead& sh, int rank) {
   return sh.order_lane;
 }
 
-template <typename T, bool ALIGNED>
+// EXACT: the launch reports row statistics (row_stats is set), so sampled
+// rows take the exact sweep; otherwise the lazy one.  One instantiation per
+// mode keeps each kernel's code to the sweep it runs.
+template <typename T, bool ALIGNED, bool EXACT>
 __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_accept_kernel(const VerifyParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SmemHead& sh = *reinterpret_cast<SmemHead*>(smem_raw);
@@ -1478,7 +1481,7 @@ __global__ void __launch_bounds__(kThreads, kConsumerWarps <= 8 ? 2 : 1) verify_
         if (lane == 0) sh.wpart[s][warp] = identity_partial();
     bool ok = true;
     // Sampled rows report their exact max and argmax only into row_stats.
-    const bool exact_stats = p.row_stats != nullptr;
+    constexpr bool exact_stats = EXACT;
     if (ALIGNED && body > 0) {
       const int nch = (body + slot_elems - 1) / slot_elems;  // chunks per row
       int cur = -1;

@@ -10,7 +10,8 @@ struct KernelVariant {
   int groups = 0;          // consumer-warp groups (ring slots come in multiples)
   int head_bytes_raw = 0;  // sizeof the shared-memory header
   int consumer_warps = 0;
-  void* kernel[4] = {nullptr, nullptr, nullptr, nullptr};  // [dtype * 2 + aligned]
+  void* kernel[4] = {nullptr, nullptr, nullptr, nullptr};        // [dtype * 2 + aligned], lazy sweep
+  void* kernel_exact[4] = {nullptr, nullptr, nullptr, nullptr};  // the same with row statistics
 };
 
 // The 20-consumer-warp builds: five groups of four (verify_w20.cu) and four

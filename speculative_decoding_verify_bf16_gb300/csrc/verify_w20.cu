@@ -22,10 +22,14 @@ KernelVariant w20_variant() {
   v.groups = specv_w20::kGroups;
   v.head_bytes_raw = static_cast<int>(sizeof(specv_w20::SmemHead));
   v.consumer_warps = specv_w20::kConsumerWarps;
-  v.kernel[0] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<float, false>);
-  v.kernel[1] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<float, true>);
-  v.kernel[2] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<specv_w20::bf16_tag, false>);
-  v.kernel[3] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<specv_w20::bf16_tag, true>);
+  v.kernel[0] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<float, false, false>);
+  v.kernel[1] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<float, true, false>);
+  v.kernel[2] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<specv_w20::bf16_tag, false, false>);
+  v.kernel[3] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<specv_w20::bf16_tag, true, false>);
+  v.kernel_exact[0] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<float, false, true>);
+  v.kernel_exact[1] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<float, true, true>);
+  v.kernel_exact[2] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<specv_w20::bf16_tag, false, true>);
+  v.kernel_exact[3] = reinterpret_cast<void*>(&specv_w20::verify_accept_kernel<specv_w20::bf16_tag, true, true>);
   return v;
 }
 
